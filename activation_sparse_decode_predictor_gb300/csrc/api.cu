@@ -1,0 +1,377 @@
+// extern "C" entry points of the sparse-FFN library: host-side validation,
+// workspace layout and kernel sequencing.  Declarations and the contract of
+// each call are in include/pi.h.
+#include <algorithm>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "internal.h"
+#include "pi.h"
+
+namespace pi {
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
+{
+    WsLayout L{};
+    size_t o = 0;
+    L.ctrl = o;
+    o += sizeof(WsCtrl);
+    L.status = o;
+    o = align256(o + (size_t)((d_ff + 31) / 32) * 8);
+    L.h = o;
+    o = align256(o + (size_t)batch * (size_t)rank * 4);
+    L.idx = o;
+    o = align256(o + (size_t)d_ff * 4);
+    L.nact = o;
+    o = align256(o + 16);
+    L.act = o;
+    if (batch > 1) o = align256(o + (size_t)d_ff * 8 * 4);
+    L.total = o;
+    (void)d_model;
+    return L;
+}
+
+size_t compact_ws_bytes(int n) { return align256(sizeof(WsCtrl) + (size_t)((n + 31) / 32) * 8); }
+
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = v > 0 ? v : 1;
+    }
+    return cache[dev];
+}
+
+ScanGeom scan_geom(int n)
+{
+    const int words = (n + 31) / 32;
+    const int target = 2 * sm_count();
+    int wpt = (words + target - 1) / target;
+    wpt = std::max(1, std::min(32, wpt));
+    ScanGeom g;
+    g.tile_rows = 32 * wpt;
+    g.ntiles = (n + g.tile_rows - 1) / g.tile_rows;
+    return g;
+}
+
+}  // namespace pi
+
+using namespace pi;
+
+namespace {
+
+inline bool al(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+inline bool overlap(const void *a, size_t an, const void *b, size_t bn)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bn && y < x + an;
+}
+
+inline pi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PI_OK : PI_ERR_CUDA; }
+
+// Checks of the FFN part (ffn) and / or the predictor part (pred) of a desc.
+pi_status check_desc(const pi_ffn_desc *D, bool ffn, bool pred)
+{
+    if (!D) return PI_ERR_NULL;
+    if (D->d_model < 8 || D->d_model > PI_MAX_D_MODEL || D->d_model % 8) return PI_ERR_SHAPE;
+    if (D->d_ff < 1 || D->d_ff >= (1 << 26)) return PI_ERR_SHAPE;
+    if (D->gated != 0 && D->gated != 1) return PI_ERR_SHAPE;
+    if (D->act != PI_ACT_RELU && D->act != PI_ACT_RELU2) return PI_ERR_SHAPE;
+    if (ffn) {
+        if (D->wtype != PI_F32 && D->wtype != PI_F16 && D->wtype != PI_Q4_0) return PI_ERR_DTYPE;
+        if (D->wtype == PI_Q4_0 && D->d_model % 256) return PI_ERR_SHAPE;
+        if (!D->w_up || !D->w_down || (D->gated && !D->w_gate)) return PI_ERR_NULL;
+        if (!al(D->w_up, 16) || !al(D->w_down, 16) || (D->gated && !al(D->w_gate, 16))) return PI_ERR_ALIGN;
+        if ((D->b_act && !al(D->b_act, 4)) || (D->b_down && !al(D->b_down, 16))) return PI_ERR_ALIGN;
+    }
+    if (pred) {
+        if (D->ptype != PI_F32 && D->ptype != PI_F16) return PI_ERR_DTYPE;
+        if (D->rank < 8 || D->rank > PI_MAX_RANK || D->rank % 8) return PI_ERR_SHAPE;
+        if (!D->p1 || !D->p2) return PI_ERR_NULL;
+        if (!al(D->p1, 16) || !al(D->p2, 16) || (D->p_bias && !al(D->p_bias, 4))) return PI_ERR_ALIGN;
+    }
+    return PI_OK;
+}
+
+pi_status check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (!ws) return PI_ERR_WORKSPACE;
+    if (!al(ws, 256)) return PI_ERR_ALIGN;
+    if (ws_bytes < need) return PI_ERR_WORKSPACE;
+    return PI_OK;
+}
+
+pi_status check_io(const pi_ffn_desc *D, const float *x, int32_t B, const float *residual, const float *y)
+{
+    if (B < 1 || B > PI_MAX_BATCH) return PI_ERR_SHAPE;
+    if (!x || !y) return PI_ERR_NULL;
+    if (!al(x, 16) || !al(y, 16) || (residual && !al(residual, 16))) return PI_ERR_ALIGN;
+    const size_t nb = (size_t)B * D->d_model * sizeof(float);
+    if (overlap(x, nb, y, nb)) return PI_ERR_ALIAS;
+    if (residual && residual != y && overlap(residual, nb, y, nb)) return PI_ERR_ALIAS;
+    if (B > 1 && D->wtype == PI_F32) return PI_ERR_DTYPE;
+    return PI_OK;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off); }
+
+pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float *logits, uint8_t *mask, int32_t *idx,
+                          int32_t *n_active, int32_t cap, void *ws, float *y_init, const float *residual,
+                          cudaStream_t s)
+{
+    const WsLayout L = ws_layout(D->d_model, D->d_ff, D->rank, B);
+    float *h = at<float>(ws, L.h);
+    cudaError_t e = launch_pred_hidden(D->ptype, D->p1, x, B, D->d_model, D->rank, h, s);
+    if (e != cudaSuccess) return PI_ERR_CUDA;
+    const ScanGeom g = scan_geom(D->d_ff);
+    PredParams p{};
+    p.p2 = D->p2;
+    p.p_bias = D->p_bias;
+    p.h = h;
+    p.B = B;
+    p.r = D->rank;
+    p.F = D->d_ff;
+    p.tau = D->threshold;
+    p.logits = logits;
+    p.mask = mask;
+    p.idx = idx;
+    p.n_active = n_active;
+    p.cap = cap;
+    p.ctrl = at<WsCtrl>(ws, L.ctrl);
+    p.status = at<unsigned long long>(ws, L.status);
+    p.ntiles = g.ntiles;
+    p.tile_rows = g.tile_rows;
+    p.y = y_init;
+    p.residual = residual;
+    p.b_down = D->b_down;
+    p.d = D->d_model;
+    return cuda_status(launch_pred_logits(D->ptype, p, s));
+}
+
+pi_status enqueue_sparse(const pi_ffn_desc *D, const float *x, int32_t B, const int32_t *idx,
+                         const int32_t *n_active, float *y, void *ws, cudaStream_t s)
+{
+    const WsLayout L = ws_layout(D->d_model, D->d_ff, D->rank, B);
+    SparseParams p{};
+    p.w_act = static_cast<const uint8_t *>(D->gated ? D->w_gate : D->w_up);
+    p.w_up = static_cast<const uint8_t *>(D->gated ? D->w_up : nullptr);
+    p.w_down = static_cast<const uint8_t *>(D->w_down);
+    p.b_act = D->b_act;
+    p.x = x;
+    p.idx = idx;
+    p.n_active = n_active;
+    p.y = y;
+    p.ctrl = at<WsCtrl>(ws, L.ctrl);
+    p.act_ws = B > 1 ? at<float>(ws, L.act) : nullptr;
+    p.d = D->d_model;
+    p.F = D->d_ff;
+    p.act = D->act;
+    p.B = B;
+    const cudaError_t e = B == 1 ? launch_sparse_b1(D->wtype, D->gated, p, s)
+                                 : launch_sparse_union(D->wtype, D->gated, p, s);
+    return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pi_status_str(int32_t st)
+{
+    switch (st) {
+    case PI_OK: return "ok";
+    case PI_ERR_NULL: return "required pointer is NULL";
+    case PI_ERR_SHAPE: return "size out of range or not divisible as required";
+    case PI_ERR_DTYPE: return "unsupported storage type";
+    case PI_ERR_ALIGN: return "pointer not aligned as required";
+    case PI_ERR_CAPACITY: return "active list exceeded its capacity";
+    case PI_ERR_CUDA: return "CUDA error";
+    case PI_ERR_TIMEOUT: return "bounded device wait gave up";
+    case PI_ERR_WORKSPACE: return "workspace missing or too small";
+    case PI_ERR_ALIAS: return "output overlaps an input";
+    case PI_ERR_INDEX: return "neuron index out of range";
+    default: return "unknown status";
+    }
+}
+
+size_t pi_workspace_bytes(const pi_ffn_desc *desc, int32_t batch)
+{
+    if (!desc || batch < 1 || batch > PI_MAX_BATCH) return 0;
+    if (desc->d_model < 8 || desc->d_ff < 1 || desc->rank < 0) return 0;
+    return ws_layout(desc->d_model, desc->d_ff, desc->rank, batch).total;
+}
+
+size_t pi_compact_workspace_bytes(int32_t n) { return n < 1 ? 0 : compact_ws_bytes(n); }
+
+pi_status pi_compact(const uint8_t *mask, int32_t n, int32_t *idx, int32_t *count, int32_t cap, void *ws,
+                     size_t ws_bytes, pi_stream stream)
+{
+    if (!mask || !idx || !count) return PI_ERR_NULL;
+    if (n < 1 || cap < 1) return PI_ERR_SHAPE;
+    if (!al(idx, 4) || !al(count, 4)) return PI_ERR_ALIGN;
+    pi_status st = check_ws(ws, ws_bytes, compact_ws_bytes(n));
+    if (st != PI_OK) return st;
+    return cuda_status(launch_compact(mask, n, idx, count, cap, at<WsCtrl>(ws, 0),
+                                      at<unsigned long long>(ws, sizeof(WsCtrl)), (cudaStream_t)stream));
+}
+
+pi_status pi_predict(const pi_ffn_desc *desc, const float *x, int32_t batch, float *logits, uint8_t *mask,
+                     int32_t *idx, int32_t *n_active, int32_t cap, void *ws, size_t ws_bytes, pi_stream stream)
+{
+    pi_status st = check_desc(desc, false, true);
+    if (st != PI_OK) return st;
+    if (batch < 1 || batch > PI_MAX_BATCH || cap < 1) return PI_ERR_SHAPE;
+    if (!x || !idx || !n_active) return PI_ERR_NULL;
+    if (!al(x, 16) || (logits && !al(logits, 4)) || !al(idx, 4) || !al(n_active, 4)) return PI_ERR_ALIGN;
+    st = check_ws(ws, ws_bytes, ws_layout(desc->d_model, desc->d_ff, desc->rank, batch).total);
+    if (st != PI_OK) return st;
+    return enqueue_predict(desc, x, batch, logits, mask, idx, n_active, cap, ws, nullptr, nullptr,
+                           (cudaStream_t)stream);
+}
+
+pi_status pi_sparse_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, const int32_t *idx,
+                        const int32_t *n_active, const float *residual, float *y, void *ws, size_t ws_bytes,
+                        pi_stream stream)
+{
+    pi_status st = check_desc(desc, true, false);
+    if (st != PI_OK) return st;
+    st = check_io(desc, x, batch, residual, y);
+    if (st != PI_OK) return st;
+    if (!idx || !n_active) return PI_ERR_NULL;
+    if (!al(idx, 4) || !al(n_active, 4)) return PI_ERR_ALIGN;
+    st = check_ws(ws, ws_bytes, ws_layout(desc->d_model, desc->d_ff, desc->rank, batch).total);
+    if (st != PI_OK) return st;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (launch_init_y(y, desc->b_down, residual, batch, desc->d_model, nullptr, nullptr, 0, s) != cudaSuccess)
+        return PI_ERR_CUDA;
+    return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s);
+}
+
+pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,
+                       int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes, pi_stream stream)
+{
+    pi_status st = check_desc(desc, true, true);
+    if (st != PI_OK) return st;
+    st = check_io(desc, x, batch, residual, y);
+    if (st != PI_OK) return st;
+    if ((idx == nullptr) != (n_active == nullptr)) return PI_ERR_NULL;
+    if ((idx && !al(idx, 4)) || (n_active && !al(n_active, 4))) return PI_ERR_ALIGN;
+    const WsLayout L = ws_layout(desc->d_model, desc->d_ff, desc->rank, batch);
+    st = check_ws(ws, ws_bytes, L.total);
+    if (st != PI_OK) return st;
+    if (!idx) {
+        idx = at<int32_t>(ws, L.idx);
+        n_active = at<int32_t>(ws, L.nact);
+    }
+    const cudaStream_t s = (cudaStream_t)stream;
+    st = enqueue_predict(desc, x, batch, nullptr, nullptr, idx, n_active, desc->d_ff, ws, y, residual, s);
+    if (st != PI_OK) return st;
+    return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s);
+}
+
+pi_status pi_dense_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,
+                       void *ws, size_t ws_bytes, pi_stream stream)
+{
+    pi_status st = check_desc(desc, true, false);
+    if (st != PI_OK) return st;
+    st = check_io(desc, x, batch, residual, y);
+    if (st != PI_OK) return st;
+    const WsLayout L = ws_layout(desc->d_model, desc->d_ff, desc->rank, batch);
+    st = check_ws(ws, ws_bytes, L.total);
+    if (st != PI_OK) return st;
+    const cudaStream_t s = (cudaStream_t)stream;
+    int32_t *idx = at<int32_t>(ws, L.idx);
+    int32_t *n = at<int32_t>(ws, L.nact);
+    if (launch_init_y(y, desc->b_down, residual, batch, desc->d_model, idx, n, desc->d_ff, s) != cudaSuccess)
+        return PI_ERR_CUDA;
+    return enqueue_sparse(desc, x, batch, idx, n, y, ws, s);
+}
+
+size_t pi_q4_0_bytes(int64_t rows, int64_t cols)
+{
+    if (rows < 1 || cols < 32 || cols % 32) return 0;
+    return (size_t)rows * (size_t)(cols / 2) + (size_t)rows * (size_t)(cols / 32) * 2;
+}
+
+pi_status pi_quantize_q4_0(const void *src, int32_t src_type, int64_t rows, int64_t cols, void *dst,
+                           pi_stream stream)
+{
+    if (!src || !dst) return PI_ERR_NULL;
+    if (src_type != PI_F32 && src_type != PI_F16) return PI_ERR_DTYPE;
+    if (rows < 1 || cols < 32 || cols % 32) return PI_ERR_SHAPE;
+    if (!al(src, 16) || !al(dst, 16)) return PI_ERR_ALIGN;
+    const size_t nsrc = (size_t)rows * cols * (src_type == PI_F32 ? 4 : 2);
+    if (overlap(src, nsrc, dst, pi_q4_0_bytes(rows, cols))) return PI_ERR_ALIAS;
+    return cuda_status(launch_quantize_q4_0(src, src_type, rows, cols, dst, (cudaStream_t)stream));
+}
+
+pi_status pi_fire_counts(const pi_ffn_desc *desc, const float *X, int32_t T, int32_t *counts, pi_stream stream)
+{
+    pi_status st = check_desc(desc, true, false);
+    if (st != PI_OK) return st;
+    if (desc->wtype == PI_Q4_0) return PI_ERR_DTYPE;
+    if (!X || !counts) return PI_ERR_NULL;
+    if (T < 1) return PI_ERR_SHAPE;
+    if (!al(X, 4) || !al(counts, 4)) return PI_ERR_ALIGN;
+    const void *w = desc->gated ? desc->w_gate : desc->w_up;
+    return cuda_status(launch_fire_counts(desc->wtype, w, desc->b_act, X, T, desc->d_model, desc->d_ff, counts,
+                                          (cudaStream_t)stream));
+}
+
+pi_status pi_hot_first_perm(const int32_t *counts, int32_t n, int32_t *perm)
+{
+    if (!counts || !perm) return PI_ERR_NULL;
+    if (n < 1) return PI_ERR_SHAPE;
+    std::vector<int32_t> order((size_t)n);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [counts](int32_t a, int32_t b) { return counts[a] > counts[b]; });
+    std::copy(order.begin(), order.end(), perm);
+    return PI_OK;
+}
+
+pi_status pi_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_bytes, const int32_t *perm,
+                          pi_stream stream)
+{
+    if (!src || !dst || !perm) return PI_ERR_NULL;
+    if (rows < 1 || row_bytes < 1) return PI_ERR_SHAPE;
+    if (!al(perm, 4)) return PI_ERR_ALIGN;
+    if (overlap(src, (size_t)(rows * row_bytes), dst, (size_t)(rows * row_bytes))) return PI_ERR_ALIAS;
+    return cuda_status(launch_permute_rows(src, dst, rows, row_bytes, perm, (cudaStream_t)stream));
+}
+
+pi_status pi_rms_residual(const float *x, const float *y, int32_t batch, int32_t d_model, float *x_next,
+                          pi_stream stream)
+{
+    if (!x || !y || !x_next) return PI_ERR_NULL;
+    if (batch < 1 || d_model < 1) return PI_ERR_SHAPE;
+    if (!al(x, 4) || !al(y, 4) || !al(x_next, 4)) return PI_ERR_ALIGN;
+    return cuda_status(launch_rms_residual(x, y, batch, d_model, x_next, (cudaStream_t)stream));
+}
+
+pi_status pi_sync_status(void *ws, size_t ws_bytes, pi_stream stream)
+{
+    if (!ws) return PI_ERR_WORKSPACE;
+    if (ws_bytes < sizeof(WsCtrl)) return PI_ERR_WORKSPACE;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return PI_ERR_CUDA;
+    unsigned err = 0;
+    if (cudaMemcpy(&err, ws, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return PI_ERR_CUDA;
+    if (err) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(ws, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess) return PI_ERR_CUDA;
+    }
+    if (err & ERR_TIMEOUT) return PI_ERR_TIMEOUT;
+    if (err & ERR_CAPACITY) return PI_ERR_CAPACITY;
+    if (err & ERR_INDEX) return PI_ERR_INDEX;
+    return PI_OK;
+}
+
+}  // extern "C"

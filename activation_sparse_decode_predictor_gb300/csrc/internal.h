@@ -1,0 +1,110 @@
+// Host-side plumbing shared by the translation units of the library: workspace
+// layout, launch geometry and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace pi {
+
+// Workspace regions, byte offsets from the workspace base (all 256-aligned).
+struct WsLayout {
+    size_t ctrl;      // WsCtrl
+    size_t status;    // scan tile status words, one per 32 neurons
+    size_t h;         // predictor hidden [batch][rank] fp32
+    size_t idx;       // internal active list [d_ff] int32
+    size_t nact;      // internal active count (int32)
+    size_t act;       // union path: activations [d_ff][8] fp32
+    size_t total;
+};
+
+WsLayout ws_layout(int d_model, int d_ff, int rank, int batch);
+size_t compact_ws_bytes(int n);
+
+// Decoupled look-back scan geometry over n entries: tile_rows (multiple of 32,
+// at most 1024) entries per tile, ntiles tiles.
+struct ScanGeom {
+    int ntiles;
+    int tile_rows;
+};
+ScanGeom scan_geom(int n);
+
+int sm_count();  // of the current device (cached per device)
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ---- predictor + compaction (predict.cu) ------------------------------------------
+struct PredParams {
+    const void *p2;
+    const float *p_bias;
+    const float *h;
+    int B, r, F;
+    float tau;
+    float *logits;        // [B][F] or null
+    uint8_t *mask;        // [F] or null
+    int *idx;
+    int *n_active;
+    int cap;
+    WsCtrl *ctrl;
+    unsigned long long *status;
+    int ntiles, tile_rows;
+    float *y;             // when non-null: y = b_down + residual is written here
+    const float *residual;
+    const float *b_down;
+    int d;
+};
+
+cudaError_t launch_pred_hidden(int ptype, const void *p1, const float *x, int B, int d, int r, float *h,
+                               cudaStream_t s);
+cudaError_t launch_pred_logits(int ptype, const PredParams &p, cudaStream_t s);
+cudaError_t launch_compact(const uint8_t *mask, int n, int *idx, int *count, int cap, WsCtrl *ctrl,
+                           unsigned long long *status, cudaStream_t s);
+
+// ---- sparse FFN (sparse_ffn.cu, union_mma.cu) --------------------------------------
+struct SparseParams {
+    const uint8_t *w_act;   // gate (gated) or up (non-gated)
+    const uint8_t *w_up;    // up, gated only
+    const uint8_t *w_down;
+    const float *b_act;
+    const float *x;         // [B][d]
+    const int *idx;
+    const int *n_active;
+    float *y;               // [B][d], already holding b_down + residual
+    WsCtrl *ctrl;
+    float *act_ws;          // union path scratch [F][8]
+    int d, F, act, B;
+};
+
+cudaError_t launch_sparse_b1(int wtype, int gated, const SparseParams &p, cudaStream_t s);
+cudaError_t launch_sparse_union(int wtype, int gated, const SparseParams &p, cudaStream_t s);
+
+// ---- small kernels (aux.cu) ------------------------------------------------------
+cudaError_t launch_init_y(float *y, const float *b_down, const float *residual, int B, int d,
+                          int *iota_idx, int *iota_n, int iota_count, cudaStream_t s);
+cudaError_t launch_quantize_q4_0(const void *src, int src_type, int64_t rows, int64_t cols, void *dst,
+                                 cudaStream_t s);
+cudaError_t launch_fire_counts(int wtype, const void *w, const float *b, const float *X, int T, int d, int F,
+                               int *counts, cudaStream_t s);
+cudaError_t launch_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_bytes, const int *perm,
+                                cudaStream_t s);
+cudaError_t launch_rms_residual(const float *x, const float *y, int B, int d, float *out, cudaStream_t s);
+
+}  // namespace pi
