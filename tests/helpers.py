@@ -24,10 +24,14 @@ def to_host(L: dict) -> dict:
 
 
 def q4_blob_random(rows: int, cols: int, seed: int) -> np.ndarray:
-    """A random Q4_0 blob whose scales are powers of two (exact products)."""
+    """A random Q4_0 blob with codes 6..10 and scales 0.5 or 1, so weights are
+    multiples of 0.5 in [-2, 2]: with small integer tokens every fp32 partial
+    sum of a layer of a few hundred neurons stays exactly representable."""
     rng = np.random.default_rng(seed)
-    codes = rng.integers(0, 256, rows * cols // 2, dtype=np.uint8)
-    scales = (2.0 ** rng.integers(-3, 2, rows * (cols // 32))).astype(np.float16).view(np.uint8)
+    lo = rng.integers(6, 11, rows * cols // 2)
+    hi = rng.integers(6, 11, rows * cols // 2)
+    codes = (lo | (hi << 4)).astype(np.uint8)
+    scales = (2.0 ** rng.integers(-1, 1, rows * (cols // 32))).astype(np.float16).view(np.uint8)
     return np.concatenate([codes, scales])
 
 
