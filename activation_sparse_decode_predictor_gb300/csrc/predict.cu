@@ -10,7 +10,7 @@
 // Kernels:
 //   k_pred_hidden  h = max(P1 x, 0): one warp per P1 row, x staged in shared
 //                  memory, 16-byte streaming loads, shuffle reduction.
-//   k_pred_logits  logit rows of P2 (one warp per row, two rows in flight),
+//   k_pred_logits  logit rows of P2 (one warp per row, four rows in flight),
 //                  threshold and union, warp-ballot mask words, then a
 //                  single-pass decoupled look-back scan across tiles (Merrill &
 //                  Garland, "Single-pass Parallel Prefix Scan with Decoupled
@@ -38,18 +38,27 @@ __device__ __forceinline__ float dot_chunk<float>(uint4 w, const float *x) { ret
 // h[b][k] = max(P1[k] . x[b], 0)
 template <typename PT>
 __global__ void __launch_bounds__(kThreads) k_pred_hidden(const PT *__restrict__ p1, const float *__restrict__ x,
-                                                          int B, int d, int r, float *__restrict__ h)
+                                                          int B, int d, int r, float *__restrict__ h,
+                                                          const uint8_t *__restrict__ p2, size_t p2_bytes)
 {
     extern __shared__ __align__(16) float xs[];  // [d]
     constexpr int EPC = 16 / sizeof(PT);
+    constexpr int U = 8;  // 16-byte loads in flight per lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kWarps + warp;
     const int nch = d / EPC;
     const uint4 *wrow = reinterpret_cast<const uint4 *>(p1 + (size_t)row * d);
 
     // The predictor weights do not depend on the previous kernel: pull this
-    // CTA's rows towards L2 while that kernel is still running.
-    if (lane == 0 && row < r) prefetch_l2(wrow, (uint32_t)(d * sizeof(PT)));
+    // CTA's P1 rows and a 1/grid slice of P2 towards L2 while that kernel is
+    // still running, so both predictor GEMVs later read L2.
+    if (lane == 0) {
+        if (row < r) prefetch_l2(wrow, (uint32_t)(d * sizeof(PT)));
+        const size_t per_cta = ((p2_bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+        const size_t piece = ((per_cta + kWarps - 1) / kWarps + 15) & ~(size_t)15;
+        const size_t off = (size_t)blockIdx.x * per_cta + (size_t)warp * piece;
+        if (off < p2_bytes) prefetch_l2(p2 + off, (uint32_t)min(piece, p2_bytes - off));
+    }
     pdl_wait();
     pdl_trigger();
 
@@ -59,13 +68,13 @@ __global__ void __launch_bounds__(kThreads) k_pred_hidden(const PT *__restrict__
         __syncthreads();
         if (row < r) {
             float acc = 0.f;
-            for (int c0 = lane; c0 < nch; c0 += 32 * 4) {
-                uint4 w[4];
+            for (int c0 = lane; c0 < nch; c0 += 32 * U) {
+                uint4 w[U];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < U; ++u)
                     if (c0 + 32 * u < nch) w[u] = ld_stream(wrow + c0 + 32 * u);
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < U; ++u)
                     if (c0 + 32 * u < nch) acc += dot_chunk<PT>(w[u], xs + (c0 + 32 * u) * EPC);
             }
             acc = warp_sum(acc);
@@ -84,34 +93,49 @@ __device__ __forceinline__ unsigned long long pack_status(unsigned epoch, unsign
 }
 
 // Returns the exclusive prefix of `tile` (number of active entries in tiles
-// before it) and publishes this tile's inclusive prefix.  Single thread.
-__device__ unsigned lookback(unsigned long long *status, int tile, unsigned count, unsigned epoch, unsigned *err)
+// before it) and publishes this tile's inclusive prefix.  Called by all 32
+// lanes of one warp: each pass reads a window of 32 predecessor status words
+// at once, so a tile resolves its prefix in about tile/32 L2 round trips even
+// when every tile finishes at the same moment.
+__device__ unsigned lookback_warp(unsigned long long *status, int tile, unsigned count, unsigned epoch, unsigned *err)
 {
+    const int lane = threadIdx.x & 31;
+    const unsigned ep = epoch & 0x3fffffffu;
     if (tile == 0) {
-        st_volatile_u64(&status[0], pack_status(epoch, 2u, count));
+        if (lane == 0) st_volatile_u64(&status[0], pack_status(epoch, 2u, count));
         return 0u;
     }
-    st_volatile_u64(&status[tile], pack_status(epoch, 1u, count));
+    if (lane == 0) st_volatile_u64(&status[tile], pack_status(epoch, 1u, count));
     unsigned excl = 0;
-    int p = tile - 1;
+    int base = tile - 1;
     long long spins = 0;
-    while (p >= 0) {
-        const unsigned long long s = ld_volatile_u64(&status[p]);
-        const unsigned tag = (unsigned)(s >> 32);
-        const unsigned flag = tag & 3u;
-        if ((tag >> 2) == (epoch & 0x3fffffffu) && flag != 0u) {
-            excl += (unsigned)s;
-            if (flag == 2u) break;
-            --p;
-        } else {
+    for (;;) {
+        const int p = base - lane;
+        unsigned flag = 2u, val = 0u;  // before tile 0: an empty inclusive prefix
+        if (p >= 0) {
+            const unsigned long long s = ld_volatile_u64(&status[p]);
+            const unsigned tag = (unsigned)(s >> 32);
+            flag = (tag >> 2) == ep ? (tag & 3u) : 0u;
+            val = (unsigned)s;
+        }
+        if (__any_sync(0xffffffffu, flag == 0u)) {
             if (++spins > kSpinLimit) {
-                atomicOr(err, ERR_TIMEOUT);
+                if (lane == 0) atomicOr(err, ERR_TIMEOUT);
                 break;
             }
             __nanosleep(32);
+            continue;
         }
+        const unsigned pm = __ballot_sync(0xffffffffu, flag == 2u);
+        const int first = pm ? __ffs(pm) - 1 : 31;
+        unsigned v = lane <= first ? val : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        excl += v;
+        if (pm) break;
+        base -= 32;
     }
-    st_volatile_u64(&status[tile], pack_status(epoch, 2u, excl + count));
+    if (lane == 0) st_volatile_u64(&status[tile], pack_status(epoch, 2u, excl + count));
     return excl;
 }
 
@@ -138,8 +162,8 @@ __device__ void scan_emit(ScanSmem &sm, int ntiles, int tile_start, int nw, int 
         }
         if (lane < nw) sm.wpre[lane] = inc - c;
         const unsigned total = __shfl_sync(0xffffffffu, inc, 31);
+        const unsigned base = lookback_warp(status, tile, total, sm.epoch, &ctrl->err);
         if (lane == 0) {
-            const unsigned base = lookback(status, tile, total, sm.epoch, &ctrl->err);
             sm.base = base;
             if (tile == ntiles - 1) {
                 unsigned all = base + total;
@@ -178,10 +202,15 @@ __device__ __forceinline__ void scan_finish(WsCtrl *ctrl, int ntiles, unsigned e
     }
 }
 
-__device__ __forceinline__ void scan_start(ScanSmem &sm, WsCtrl *ctrl)
+__device__ __forceinline__ void scan_start(ScanSmem &sm, WsCtrl *ctrl, int ntiles)
 {
     if (threadIdx.x == 0) {
-        sm.tile = atomicAdd(&ctrl->ticket, 1u);
+        unsigned t = atomicAdd(&ctrl->ticket, 1u);
+        if (t >= (unsigned)ntiles) {  // a workspace that was not zero-filled: stay in bounds, report it
+            atomicOr(&ctrl->err, ERR_TIMEOUT);
+            t %= (unsigned)ntiles;
+        }
+        sm.tile = t;
         sm.epoch = *reinterpret_cast<volatile unsigned *>(&ctrl->epoch);
     }
 }
@@ -195,30 +224,14 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
     constexpr int EPC = 16 / sizeof(PT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nch = p.r / EPC;
-    const size_t rowbytes = (size_t)p.r * sizeof(PT);
     float *hs = dsm;                          // [B][r]
     float *lg = dsm + (size_t)p.B * p.r;      // [NB][tile_rows]
     const PT *p2 = static_cast<const PT *>(p.p2);
 
-    // Prologue, independent of the predecessor: prefetch the P2 rows of tile
-    // blockIdx.x into L2 (each warp a contiguous eighth).  Tickets hand tiles
-    // out in start order, so this is the tile this CTA gets, or close to it.
-    {
-        const int r0 = blockIdx.x * p.tile_rows;
-        const int r1 = min(r0 + p.tile_rows, p.F);
-        if (r0 < r1 && lane == 0) {
-            const size_t bytes = (size_t)(r1 - r0) * rowbytes;
-            const size_t piece = ((bytes + kWarps - 1) / kWarps + 15) & ~(size_t)15;
-            const size_t off = (size_t)warp * piece;
-            if (off < bytes) {
-                const size_t len = min(piece, bytes - off);
-                prefetch_l2(reinterpret_cast<const uint8_t *>(p2 + (size_t)r0 * p.r) + off, (uint32_t)len);
-            }
-        }
-    }
+    // P2 was pulled towards L2 by the hidden-layer kernel's prologue.
     pdl_wait();
     pdl_trigger();
-    scan_start(sm, p.ctrl);
+    scan_start(sm, p.ctrl, p.ntiles);
     {
         const float4 *h4 = reinterpret_cast<const float4 *>(p.h);
         for (int i = threadIdx.x; i < p.B * p.r / 4; i += kThreads) reinterpret_cast<float4 *>(hs)[i] = h4[i];
@@ -228,24 +241,30 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
     const int tile_start = tile * p.tile_rows;
     const int nrows = min(p.tile_rows, p.F - tile_start);
 
-    for (int rr = warp; rr < nrows; rr += 2 * kWarps) {
-        const int ra = rr, rb = rr + kWarps;
-        const bool hasb = rb < nrows;
-        const uint4 *wa = reinterpret_cast<const uint4 *>(p2 + (size_t)(tile_start + ra) * p.r);
-        const uint4 *wb = reinterpret_cast<const uint4 *>(p2 + (size_t)(tile_start + (hasb ? rb : ra)) * p.r);
-        float acc_a[NB], acc_b[NB];
+    constexpr int RW = 4;  // rows in flight per warp
+    for (int rr = warp; rr < nrows; rr += RW * kWarps) {
+        const uint4 *wp[RW];
+        bool ok[RW];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) acc_a[b] = acc_b[b] = 0.f;
+        for (int i = 0; i < RW; ++i) {
+            const int row = rr + i * kWarps;
+            ok[i] = row < nrows;
+            wp[i] = reinterpret_cast<const uint4 *>(p2 + (size_t)(tile_start + (ok[i] ? row : rr)) * p.r);
+        }
+        float acc[RW][NB];
+#pragma unroll
+        for (int i = 0; i < RW; ++i)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
         for (int c0 = lane; c0 < nch; c0 += 32 * 4) {
-            uint4 va[4], vb[4];
+            uint4 v[RW][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + 32 * u;
-                if (c < nch) {
-                    va[u] = ld_stream(wa + c);
-                    vb[u] = ld_stream(wb + c);
+            for (int i = 0; i < RW; ++i)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (ok[i] && c < nch) v[i][u] = ld_stream(wp[i] + c);
                 }
-            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c = c0 + 32 * u;
@@ -253,27 +272,27 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
                         if (b < p.B) {
-                            acc_a[b] += dot_chunk<PT>(va[u], hs + (size_t)b * p.r + c * EPC);
-                            acc_b[b] += dot_chunk<PT>(vb[u], hs + (size_t)b * p.r + c * EPC);
+                            const float *hb = hs + (size_t)b * p.r + c * EPC;
+#pragma unroll
+                            for (int i = 0; i < RW; ++i)
+                                if (ok[i]) acc[i][b] += dot_chunk<PT>(v[i][u], hb);
                         }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if (b < p.B) {
-                const float sa = warp_sum(acc_a[b]);
-                const float sb = warp_sum(acc_b[b]);
-                if (lane == 0) {
-                    const int ja = tile_start + ra, jb = tile_start + rb;
-                    const float la = sa + (p.p_bias ? p.p_bias[ja] : 0.f);
-                    lg[b * p.tile_rows + ra] = la;
-                    if (p.logits) p.logits[(size_t)b * p.F + ja] = la;
-                    if (hasb) {
-                        const float lb = sb + (p.p_bias ? p.p_bias[jb] : 0.f);
-                        lg[b * p.tile_rows + rb] = lb;
-                        if (p.logits) p.logits[(size_t)b * p.F + jb] = lb;
+        for (int i = 0; i < RW; ++i) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (b < p.B) {
+                    const float sum = warp_sum(acc[i][b]);
+                    const int row = rr + i * kWarps;
+                    if (lane == 0 && ok[i]) {
+                        const int j = tile_start + row;
+                        const float l = sum + (p.p_bias ? p.p_bias[j] : 0.f);
+                        lg[b * p.tile_rows + row] = l;
+                        if (p.logits) p.logits[(size_t)b * p.F + j] = l;
                     }
                 }
             }
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) k_compact(const uint8_t *__restrict_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
-    scan_start(sm, ctrl);
+    scan_start(sm, ctrl, ntiles);
     __syncthreads();
     const int tile_start = (int)sm.tile * tile_rows;
     const int nrows = min(tile_rows, n - tile_start);
@@ -350,18 +369,20 @@ __global__ void __launch_bounds__(kThreads) k_compact(const uint8_t *__restrict_
 
 // ---------------------------------------------------------------------------------
 cudaError_t launch_pred_hidden(int ptype, const void *p1, const float *x, int B, int d, int r, float *h,
-                               cudaStream_t s)
+                               const void *p2, size_t p2_bytes, cudaStream_t s)
 {
     const dim3 grid((r + kWarps - 1) / kWarps);
     const size_t smem = (size_t)d * sizeof(float);
     if (ptype == 1) {
         auto k = k_pred_hidden<__half>;
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        return launch_pdl(k, grid, dim3(kThreads), smem, s, static_cast<const __half *>(p1), x, B, d, r, h);
+        return launch_pdl(k, grid, dim3(kThreads), smem, s, static_cast<const __half *>(p1), x, B, d, r, h,
+                          static_cast<const uint8_t *>(p2), p2_bytes);
     }
     auto k = k_pred_hidden<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return launch_pdl(k, grid, dim3(kThreads), smem, s, static_cast<const float *>(p1), x, B, d, r, h);
+    return launch_pdl(k, grid, dim3(kThreads), smem, s, static_cast<const float *>(p1), x, B, d, r, h,
+                      static_cast<const uint8_t *>(p2), p2_bytes);
 }
 
 template <typename PT>

@@ -142,7 +142,8 @@ def make_layer(d_model: int, d_ff: int, rank: int, *, gated: bool, wtype: str = 
     elif predictor == "projection":
         k = rank // 2
         g = randn((d_model, k), 1.0, sd + 5, dev)
-        q, _ = torch.linalg.qr(g)                   # [d, k] orthonormal columns
+        q, _ = torch.linalg.qr(g.cpu())             # [d, k] orthonormal columns (host LAPACK)
+        q = q.to(dev)
         Q = q.T.contiguous()                        # [k, d]
         Lm = w_act_st @ Q.T                         # [d_ff, k]
         s = Lm.norm(dim=1, keepdim=True).clamp_min(1e-12)

@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle sample")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="decode tokens per step (default: the workload's)")
+    ap.add_argument("--quick", action="store_true", help="main timed step only (for profiling runs)")
     return ap.parse_args()
 
 
@@ -293,6 +295,8 @@ def run_ours(args, w):
     torch.cuda.set_device(dev)
     B.lib()
     L0, reps, X = setup_ours(w, args.replicas, dev)
+    if args.tokens:
+        X = X[:args.tokens].contiguous()
     T = X.shape[0]
     d = w.d_model
     stream = torch.cuda.Stream()
@@ -320,6 +324,15 @@ def run_ours(args, w):
         ms_step = float(tt.item())
     us_tok = ms_step * 1000.0 / (T * world)          # whole job: all ranks' tokens in the max time
 
+    peak, peak_src = measured_peaks()
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": "us_per_ffn_layer_per_token", "value": us_tok, "unit": "us/layer/token",
+                              "quick": True, "workload": w.name, "tokens_per_step": T,
+                              "layer_gbs": mean_bytes / (us_tok * world * 1e-6) / 1e9,
+                              "device_status": B.pi_sync_status(ws)}))
+        return 0
+
     # the dominant kernel alone: the sparse FFN on the predicted lists (same rotation)
     def sparse_only():
         for t in range(T):
@@ -336,7 +349,6 @@ def run_ours(args, w):
     ms_pr = time_graph(g_pr, ksteps, args.warmup, stream) / ksteps
     us_sp = ms_sp * 1000.0 / T
     us_pr = ms_pr * 1000.0 / T
-    peak, peak_src = measured_peaks()
     ffn_gbs = float(np.mean(ffn_b)) / (us_sp * 1e-6) / 1e9
     pred_gbs = float(pred_b) / (us_pr * 1e-6) / 1e9
     layer_gbs = mean_bytes / (us_tok * world * 1e-6) / 1e9
