@@ -131,7 +131,8 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
     const WsLayout L = ws_layout(D->d_model, D->d_ff, D->rank, B);
     float *h = at<float>(ws, L.h);
     const size_t p2_bytes = (size_t)D->d_ff * D->rank * (D->ptype == PI_F16 ? 2 : 4);
-    cudaError_t e = launch_pred_hidden(D->ptype, D->p1, x, B, D->d_model, D->rank, h, D->p2, p2_bytes, s);
+    cudaError_t e = launch_pred_hidden(D->ptype, D->p1, x, B, D->d_model, D->rank, h, D->p2, p2_bytes, D->p_bias,
+                                       D->b_act, D->d_ff, s);
     if (e != cudaSuccess) return PI_ERR_CUDA;
     const ScanGeom g = scan_geom(D->d_ff);
     PredParams p{};

@@ -73,7 +73,8 @@ struct PredParams {
 };
 
 cudaError_t launch_pred_hidden(int ptype, const void *p1, const float *x, int B, int d, int r, float *h,
-                               const void *p2, size_t p2_bytes, cudaStream_t s);
+                               const void *p2, size_t p2_bytes, const float *p_bias, const float *b_act, int F,
+                               cudaStream_t s);
 cudaError_t launch_pred_logits(int ptype, const PredParams &p, cudaStream_t s);
 cudaError_t launch_compact(const uint8_t *mask, int n, int *idx, int *count, int cap, WsCtrl *ctrl,
                            unsigned long long *status, cudaStream_t s);

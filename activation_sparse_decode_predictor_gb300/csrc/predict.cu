@@ -36,10 +36,25 @@ __device__ __forceinline__ float dot_chunk<float>(uint4 w, const float *x) { ret
 
 // ---------------------------------------------------------------------------------
 // h[b][k] = max(P1[k] . x[b], 0)
+// Small per-neuron vectors (p_bias, b_act): pull into L2 in 16-byte-aligned
+// pieces, split over the CTAs of the grid.
+__device__ __forceinline__ void prefetch_vec_l2(const float *v, int n)
+{
+    if (!v || n <= 0) return;
+    const uintptr_t a0 = ((uintptr_t)v + 15) & ~(uintptr_t)15;
+    const uintptr_t a1 = ((uintptr_t)(v + n)) & ~(uintptr_t)15;
+    if (a1 <= a0) return;
+    const size_t bytes = a1 - a0;
+    const size_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+    const size_t off = (size_t)blockIdx.x * per;
+    if (off < bytes) prefetch_l2(reinterpret_cast<const void *>(a0 + off), (uint32_t)min(per, bytes - off));
+}
+
 template <typename PT>
 __global__ void __launch_bounds__(kThreads) k_pred_hidden(const PT *__restrict__ p1, const float *__restrict__ x,
                                                           int B, int d, int r, float *__restrict__ h,
-                                                          const uint8_t *__restrict__ p2, size_t p2_bytes)
+                                                          const uint8_t *__restrict__ p2, size_t p2_bytes,
+                                                          const float *p_bias, const float *b_act, int F)
 {
     extern __shared__ __align__(16) float xs[];  // [d]
     constexpr int EPC = 16 / sizeof(PT);
@@ -58,6 +73,9 @@ __global__ void __launch_bounds__(kThreads) k_pred_hidden(const PT *__restrict__
         const size_t piece = ((per_cta + kWarps - 1) / kWarps + 15) & ~(size_t)15;
         const size_t off = (size_t)blockIdx.x * per_cta + (size_t)warp * piece;
         if (off < p2_bytes) prefetch_l2(p2 + off, (uint32_t)min(piece, p2_bytes - off));
+        // the per-neuron biases the logit kernel and the sparse FFN will read
+        if (warp == 0) prefetch_vec_l2(p_bias, F);
+        if (warp == 1) prefetch_vec_l2(b_act, F);
     }
     pdl_wait();
     pdl_trigger();
@@ -226,6 +244,7 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
     const int nch = p.r / EPC;
     float *hs = dsm;                          // [B][r]
     float *lg = dsm + (size_t)p.B * p.r;      // [NB][tile_rows]
+    float *pb = lg + (size_t)NB * p.tile_rows; // [tile_rows]
     const PT *p2 = static_cast<const PT *>(p.p2);
 
     // P2 was pulled towards L2 by the hidden-layer kernel's prologue.
@@ -240,6 +259,8 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
     const int tile = (int)sm.tile;
     const int tile_start = tile * p.tile_rows;
     const int nrows = min(p.tile_rows, p.F - tile_start);
+    for (int i = threadIdx.x; i < nrows; i += kThreads) pb[i] = p.p_bias ? p.p_bias[tile_start + i] : 0.f;
+    __syncthreads();
 
     constexpr int RW = 4;  // rows in flight per warp
     for (int rr = warp; rr < nrows; rr += RW * kWarps) {
@@ -290,7 +311,7 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
                     const int row = rr + i * kWarps;
                     if (lane == 0 && ok[i]) {
                         const int j = tile_start + row;
-                        const float l = sum + (p.p_bias ? p.p_bias[j] : 0.f);
+                        const float l = sum + pb[row];
                         lg[b * p.tile_rows + row] = l;
                         if (p.logits) p.logits[(size_t)b * p.F + j] = l;
                     }
@@ -369,7 +390,8 @@ __global__ void __launch_bounds__(kThreads) k_compact(const uint8_t *__restrict_
 
 // ---------------------------------------------------------------------------------
 cudaError_t launch_pred_hidden(int ptype, const void *p1, const float *x, int B, int d, int r, float *h,
-                               const void *p2, size_t p2_bytes, cudaStream_t s)
+                               const void *p2, size_t p2_bytes, const float *p_bias, const float *b_act, int F,
+                               cudaStream_t s)
 {
     const dim3 grid((r + kWarps - 1) / kWarps);
     const size_t smem = (size_t)d * sizeof(float);
@@ -377,18 +399,18 @@ cudaError_t launch_pred_hidden(int ptype, const void *p1, const float *x, int B,
         auto k = k_pred_hidden<__half>;
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         return launch_pdl(k, grid, dim3(kThreads), smem, s, static_cast<const __half *>(p1), x, B, d, r, h,
-                          static_cast<const uint8_t *>(p2), p2_bytes);
+                          static_cast<const uint8_t *>(p2), p2_bytes, p_bias, b_act, F);
     }
     auto k = k_pred_hidden<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return launch_pdl(k, grid, dim3(kThreads), smem, s, static_cast<const float *>(p1), x, B, d, r, h,
-                      static_cast<const uint8_t *>(p2), p2_bytes);
+                      static_cast<const uint8_t *>(p2), p2_bytes, p_bias, b_act, F);
 }
 
 template <typename PT>
 static cudaError_t pred_logits_nb(const PredParams &p, cudaStream_t s)
 {
-    const size_t smem = ((size_t)p.B * p.r + (size_t)8 * p.tile_rows) * sizeof(float);
+    const size_t smem = ((size_t)p.B * p.r + (size_t)9 * p.tile_rows) * sizeof(float);
     void (*k)(PredParams);
     if (p.B <= 1)
         k = k_pred_logits<PT, 1>;
