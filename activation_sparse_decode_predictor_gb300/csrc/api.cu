@@ -49,18 +49,6 @@ int sm_count()
     return cache[dev];
 }
 
-ScanGeom scan_geom(int n)
-{
-    const int words = (n + 31) / 32;
-    const int target = 2 * sm_count();
-    int wpt = (words + target - 1) / target;
-    wpt = std::max(1, std::min(32, wpt));
-    ScanGeom g;
-    g.tile_rows = 32 * wpt;
-    g.ntiles = (n + g.tile_rows - 1) / g.tile_rows;
-    return g;
-}
-
 }  // namespace pi
 
 using namespace pi;
@@ -95,6 +83,7 @@ pi_status check_desc(const pi_ffn_desc *D, bool ffn, bool pred)
     if (pred) {
         if (D->ptype != PI_F32 && D->ptype != PI_F16) return PI_ERR_DTYPE;
         if (D->rank < 8 || D->rank > PI_MAX_RANK || D->rank % 8) return PI_ERR_SHAPE;
+        if (D->d_ff >= (1 << 23)) return PI_ERR_SHAPE;
         if (!D->p1 || !D->p2) return PI_ERR_NULL;
         if (!al(D->p1, 16) || !al(D->p2, 16) || (D->p_bias && !al(D->p_bias, 4))) return PI_ERR_ALIGN;
     }
@@ -134,7 +123,6 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
     cudaError_t e = launch_pred_hidden(D->ptype, D->p1, x, B, D->d_model, D->rank, h, D->p2, p2_bytes, D->p_bias,
                                        D->b_act, D->d_ff, s);
     if (e != cudaSuccess) return PI_ERR_CUDA;
-    const ScanGeom g = scan_geom(D->d_ff);
     PredParams p{};
     p.p2 = D->p2;
     p.p_bias = D->p_bias;
@@ -150,8 +138,6 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
     p.cap = cap;
     p.ctrl = at<WsCtrl>(ws, L.ctrl);
     p.status = at<unsigned long long>(ws, L.status);
-    p.ntiles = g.ntiles;
-    p.tile_rows = g.tile_rows;
     p.y = y_init;
     p.residual = residual;
     p.b_down = D->b_down;

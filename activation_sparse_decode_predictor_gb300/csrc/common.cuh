@@ -20,9 +20,9 @@ constexpr long long kSpinLimit = 1ll << 22;
 // First 256 bytes of a workspace.
 struct WsCtrl {
     unsigned err;      // ERR_* bits, cleared by pi_sync_status
-    unsigned ticket;   // scan: next logical tile of the running launch
-    unsigned done;     // scan: tiles finished in the running launch
-    unsigned epoch;    // scan: launch generation, tags tile status words
+    unsigned spare;
+    unsigned done;     // scan: CTAs finished in the running launch
+    unsigned epoch;    // scan: launch generation, tags the CTA status words
     unsigned pad[60];
 };
 static_assert(sizeof(WsCtrl) == 256, "control block is 256 bytes");
@@ -143,15 +143,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Returns false
-// (after raising ERR_TIMEOUT) when the bound is hit.
+// Bounded wait for the phase with the given parity to complete (try_wait
+// itself suspends the thread for a while before reporting "not yet").  Returns
+// false (after raising ERR_TIMEOUT) when the bound is hit.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *err)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    for (long long i = 0; i < kSpinLimit; ++i) {
+    for (long long i = 0; i < kSpinLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
-        __nanosleep(64);
-    }
     atomicOr(err, ERR_TIMEOUT);
     return false;
 }

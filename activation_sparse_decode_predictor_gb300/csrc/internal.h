@@ -24,14 +24,6 @@ struct WsLayout {
 WsLayout ws_layout(int d_model, int d_ff, int rank, int batch);
 size_t compact_ws_bytes(int n);
 
-// Decoupled look-back scan geometry over n entries: tile_rows (multiple of 32,
-// at most 1024) entries per tile, ntiles tiles.
-struct ScanGeom {
-    int ntiles;
-    int tile_rows;
-};
-ScanGeom scan_geom(int n);
-
 int sm_count();  // of the current device (cached per device)
 
 template <typename... KArgs, typename... Args>
@@ -65,7 +57,6 @@ struct PredParams {
     int cap;
     WsCtrl *ctrl;
     unsigned long long *status;
-    int ntiles, tile_rows;
     float *y;             // when non-null: y = b_down + residual is written here
     const float *residual;
     const float *b_down;

@@ -10,14 +10,16 @@
 // Kernels:
 //   k_pred_hidden  h = max(P1 x, 0): one warp per P1 row, x staged in shared
 //                  memory, 16-byte streaming loads, shuffle reduction.
-//   k_pred_logits  logit rows of P2 (one warp per row, four rows in flight),
-//                  threshold and union, warp-ballot mask words, then a
-//                  single-pass decoupled look-back scan across tiles (Merrill &
-//                  Garland, "Single-pass Parallel Prefix Scan with Decoupled
-//                  Look-back", 2016) that writes the ascending active list.
+//   k_pred_logits  one CTA per SM over a balanced contiguous neuron range:
+//                  logit rows of P2 (one warp per row, four rows in flight,
+//                  P2 already pulled into L2 by k_pred_hidden), threshold and
+//                  union, warp-ballot mask words, then a single-pass scan
+//                  across CTAs (each publishes its count and sums those of
+//                  the CTAs before it) that writes the ascending active list.
 //   k_compact      the same scan over a caller-given byte mask.
-// Both scan kernels take their logical tile from a ticket counter, so a tile
-// only ever waits on tiles that started before it; every wait is bounded.
+// Every cross-CTA wait is bounded.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace pi {
@@ -103,116 +105,111 @@ __global__ void __launch_bounds__(kThreads) k_pred_hidden(const PT *__restrict__
 }
 
 // ---------------------------------------------------------------------------------
-// Decoupled look-back.  Tile status word: high 32 bits = (epoch << 2) | flag
-// (flag 1: tile aggregate, 2: inclusive prefix), low 32 bits = the value.
-__device__ __forceinline__ unsigned long long pack_status(unsigned epoch, unsigned flag, unsigned v)
+// Cross-CTA scan.  CTA c owns the contiguous neuron range [c*F/G, (c+1)*F/G)
+// and G never exceeds the number of SMs, so every CTA of the grid is resident
+// at once.  Each CTA publishes its active count in a status word tagged with
+// the launch's epoch, then sums the counts of all CTAs before it, read in one
+// parallel pass (G <= #SMs words) and re-polled, with a bound, only where a
+// predecessor has not published yet.  The last CTA to finish moves the epoch
+// on, so stale words of earlier launches are never mistaken for current ones.
+__device__ __forceinline__ unsigned long long pack_status(unsigned epoch, unsigned v)
 {
-    return ((unsigned long long)(((epoch & 0x3fffffffu) << 2) | flag) << 32) | v;
+    return ((unsigned long long)(((epoch & 0x7fffffffu) << 1) | 1u) << 32) | v;
 }
 
-// Returns the exclusive prefix of `tile` (number of active entries in tiles
-// before it) and publishes this tile's inclusive prefix.  Called by all 32
-// lanes of one warp: each pass reads a window of 32 predecessor status words
-// at once, so a tile resolves its prefix in about tile/32 L2 round trips even
-// when every tile finishes at the same moment.
-__device__ unsigned lookback_warp(unsigned long long *status, int tile, unsigned count, unsigned epoch, unsigned *err)
+template <int NT>
+__device__ __forceinline__ unsigned block_sum(unsigned v, unsigned *red)
 {
-    const int lane = threadIdx.x & 31;
-    const unsigned ep = epoch & 0x3fffffffu;
-    if (tile == 0) {
-        if (lane == 0) st_volatile_u64(&status[0], pack_status(epoch, 2u, count));
-        return 0u;
-    }
-    if (lane == 0) st_volatile_u64(&status[tile], pack_status(epoch, 1u, count));
-    unsigned excl = 0;
-    int base = tile - 1;
-    long long spins = 0;
-    for (;;) {
-        const int p = base - lane;
-        unsigned flag = 2u, val = 0u;  // before tile 0: an empty inclusive prefix
-        if (p >= 0) {
-            const unsigned long long s = ld_volatile_u64(&status[p]);
-            const unsigned tag = (unsigned)(s >> 32);
-            flag = (tag >> 2) == ep ? (tag & 3u) : 0u;
-            val = (unsigned)s;
-        }
-        if (__any_sync(0xffffffffu, flag == 0u)) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    unsigned t = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) t += red[w];
+    return t;
+}
+
+template <int NT>
+__device__ unsigned sum_before(unsigned long long *status, int c, unsigned count, unsigned epoch, unsigned *err,
+                               unsigned *red)
+{
+    const unsigned want = ((epoch & 0x7fffffffu) << 1) | 1u;
+    if (threadIdx.x == 0) st_volatile_u64(&status[c], pack_status(epoch, count));
+    unsigned part = 0;
+    for (int i = threadIdx.x; i < c; i += NT) {
+        unsigned long long s = ld_volatile_u64(&status[i]);
+        long long spins = 0;
+        while ((unsigned)(s >> 32) != want) {
             if (++spins > kSpinLimit) {
-                if (lane == 0) atomicOr(err, ERR_TIMEOUT);
+                atomicOr(err, ERR_TIMEOUT);
+                s = 0;
                 break;
             }
             __nanosleep(32);
-            continue;
+            s = ld_volatile_u64(&status[i]);
         }
-        const unsigned pm = __ballot_sync(0xffffffffu, flag == 2u);
-        const int first = pm ? __ffs(pm) - 1 : 31;
-        unsigned v = lane <= first ? val : 0u;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        excl += v;
-        if (pm) break;
-        base -= 32;
+        part += (unsigned)s;
     }
-    if (lane == 0) st_volatile_u64(&status[tile], pack_status(epoch, 2u, excl + count));
-    return excl;
+    return block_sum<NT>(part, red);
 }
 
-struct ScanSmem {
-    unsigned words[32];
-    unsigned wpre[32];
-    unsigned tile, epoch, base;
-};
-
-// Given this tile's mask words (smem), find its offset and write its entries
-// of the ascending active list; the last tile writes the total.  All threads.
-__device__ void scan_emit(ScanSmem &sm, int ntiles, int tile_start, int nw, int *idx, int *n_active, int cap,
-                          WsCtrl *ctrl, unsigned long long *status)
+// Exclusive prefix of popc(words[0..nw)) into wpre; returns the total.
+template <int NT>
+__device__ unsigned scan_words(const unsigned *words, unsigned *wpre, int nw, unsigned *red)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = (int)sm.tile;
-    if (warp == 0) {
-        const unsigned c = lane < nw ? __popc(sm.words[lane]) : 0u;
-        unsigned inc = c;
+    const int per = (nw + NT - 1) / NT;
+    const int w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
+    unsigned mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(words[w]);
+    unsigned inc = mine;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned t = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += t;
-        }
-        if (lane < nw) sm.wpre[lane] = inc - c;
-        const unsigned total = __shfl_sync(0xffffffffu, inc, 31);
-        const unsigned base = lookback_warp(status, tile, total, sm.epoch, &ctrl->err);
-        if (lane == 0) {
-            sm.base = base;
-            if (tile == ntiles - 1) {
-                unsigned all = base + total;
-                if (all > (unsigned)cap) {
-                    atomicOr(&ctrl->err, ERR_CAPACITY);
-                    all = (unsigned)cap;
-                }
-                *n_active = (int)all;
-            }
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
     }
     __syncthreads();
-    const unsigned base = sm.base;
-    for (int wd = warp; wd < nw; wd += kWarps) {
-        const unsigned bits = sm.words[wd];
+    if (lane == 31) red[warp] = inc;
+    __syncthreads();
+    unsigned before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        if (w < warp) before += red[w];
+        total += red[w];
+    }
+    unsigned run = before + inc - mine;
+    for (int w = w0; w < w1; ++w) {
+        wpre[w] = run;
+        run += __popc(words[w]);
+    }
+    __syncthreads();
+    return total;
+}
+
+// Write this CTA's entries of the ascending active list.
+template <int NT>
+__device__ void emit_idx(const unsigned *words, const unsigned *wpre, int nw, int row0, unsigned base, int *idx,
+                         int cap)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int wd = warp; wd < nw; wd += NT / 32) {
+        const unsigned bits = words[wd];
         if ((bits >> lane) & 1u) {
-            const unsigned pos = base + sm.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
-            if (pos < (unsigned)cap) idx[pos] = tile_start + wd * 32 + lane;
+            const unsigned pos = base + wpre[wd] + __popc(bits & ((1u << lane) - 1u));
+            if (pos < (unsigned)cap) idx[pos] = row0 + wd * 32 + lane;
         }
     }
 }
 
-// The last CTA of a launch to finish resets the ticket counters and moves the
-// epoch on, so the next launch starts from a clean scan state.
-__device__ __forceinline__ void scan_finish(WsCtrl *ctrl, int ntiles, unsigned epoch)
+__device__ __forceinline__ void scan_finish(WsCtrl *ctrl, int G, unsigned epoch)
 {
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned d = atomicAdd(&ctrl->done, 1u);
-        if (d == (unsigned)ntiles - 1u) {
-            ctrl->ticket = 0u;
+        if (d == (unsigned)G - 1u) {
             ctrl->done = 0u;
             __threadfence();
             atomicExch(&ctrl->epoch, epoch + 1u);
@@ -220,132 +217,148 @@ __device__ __forceinline__ void scan_finish(WsCtrl *ctrl, int ntiles, unsigned e
     }
 }
 
-__device__ __forceinline__ void scan_start(ScanSmem &sm, WsCtrl *ctrl, int ntiles)
+__device__ __forceinline__ void write_total(int c, int G, unsigned base, unsigned count, int *n_active, int cap,
+                                            unsigned *err)
 {
-    if (threadIdx.x == 0) {
-        unsigned t = atomicAdd(&ctrl->ticket, 1u);
-        if (t >= (unsigned)ntiles) {  // a workspace that was not zero-filled: stay in bounds, report it
-            atomicOr(&ctrl->err, ERR_TIMEOUT);
-            t %= (unsigned)ntiles;
+    if (threadIdx.x == 0 && c == G - 1) {
+        unsigned all = base + count;
+        if (all > (unsigned)cap) {
+            atomicOr(err, ERR_CAPACITY);
+            all = (unsigned)cap;
         }
-        sm.tile = t;
-        sm.epoch = *reinterpret_cast<volatile unsigned *>(&ctrl->epoch);
+        *n_active = (int)all;
     }
 }
 
+constexpr int kLThreads = 512;          // logit kernel: 16 warps per CTA, one CTA per SM
+constexpr int kLWarps = kLThreads / 32;
+constexpr int kChunk = 1024;            // rows per logits chunk held in shared memory
+
 // ---------------------------------------------------------------------------------
 template <typename PT, int NB>
-__global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
+__global__ void __launch_bounds__(kLThreads, 1) k_pred_logits(PredParams p)
 {
     extern __shared__ __align__(16) float dsm[];
-    __shared__ ScanSmem sm;
+    __shared__ unsigned red[kLWarps];
+    __shared__ unsigned s_epoch;
     constexpr int EPC = 16 / sizeof(PT);
+    constexpr int RW = 4;  // rows in flight per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int r0 = (int)((long long)p.F * c / G);
+    const int R = (int)((long long)p.F * (c + 1) / G) - r0;
+    const int nw = (R + 31) >> 5;
     const int nch = p.r / EPC;
-    float *hs = dsm;                          // [B][r]
-    float *lg = dsm + (size_t)p.B * p.r;      // [NB][tile_rows]
-    float *pb = lg + (size_t)NB * p.tile_rows; // [tile_rows]
+    float *hs = dsm;                                   // [B][r]
+    float *lg = hs + (size_t)p.B * p.r;                // [NB][kChunk]
+    float *pb = lg + (size_t)NB * kChunk;              // [kChunk]
+    unsigned *words = reinterpret_cast<unsigned *>(pb + kChunk);  // [nw]
+    unsigned *wpre = words + nw;                                  // [nw]
     const PT *p2 = static_cast<const PT *>(p.p2);
 
-    // P2 was pulled towards L2 by the hidden-layer kernel's prologue.
+    // Prologue, independent of the predecessor: the first chunk's biases.
+    for (int i = threadIdx.x; i < min(R, kChunk); i += kLThreads) pb[i] = p.p_bias ? p.p_bias[r0 + i] : 0.f;
     pdl_wait();
     pdl_trigger();
-    scan_start(sm, p.ctrl, p.ntiles);
+    if (threadIdx.x == 0) s_epoch = *reinterpret_cast<volatile unsigned *>(&p.ctrl->epoch);
     {
         const float4 *h4 = reinterpret_cast<const float4 *>(p.h);
-        for (int i = threadIdx.x; i < p.B * p.r / 4; i += kThreads) reinterpret_cast<float4 *>(hs)[i] = h4[i];
+        for (int i = threadIdx.x; i < p.B * p.r / 4; i += kLThreads) reinterpret_cast<float4 *>(hs)[i] = h4[i];
     }
     __syncthreads();
-    const int tile = (int)sm.tile;
-    const int tile_start = tile * p.tile_rows;
-    const int nrows = min(p.tile_rows, p.F - tile_start);
-    for (int i = threadIdx.x; i < nrows; i += kThreads) pb[i] = p.p_bias ? p.p_bias[tile_start + i] : 0.f;
-    __syncthreads();
 
-    constexpr int RW = 4;  // rows in flight per warp
-    for (int rr = warp; rr < nrows; rr += RW * kWarps) {
-        const uint4 *wp[RW];
-        bool ok[RW];
-#pragma unroll
-        for (int i = 0; i < RW; ++i) {
-            const int row = rr + i * kWarps;
-            ok[i] = row < nrows;
-            wp[i] = reinterpret_cast<const uint4 *>(p2 + (size_t)(tile_start + (ok[i] ? row : rr)) * p.r);
+    for (int ch0 = 0; ch0 < R; ch0 += kChunk) {
+        const int cn = min(kChunk, R - ch0);
+        if (ch0 > 0) {
+            for (int i = threadIdx.x; i < cn; i += kLThreads) pb[i] = p.p_bias ? p.p_bias[r0 + ch0 + i] : 0.f;
+            __syncthreads();
         }
-        float acc[RW][NB];
+        for (int rr = warp; rr < cn; rr += RW * kLWarps) {
+            const uint4 *wp[RW];
+            bool ok[RW];
 #pragma unroll
-        for (int i = 0; i < RW; ++i)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
-        for (int c0 = lane; c0 < nch; c0 += 32 * 4) {
-            uint4 v[RW][4];
+            for (int i = 0; i < RW; ++i) {
+                const int row = rr + i * kLWarps;
+                ok[i] = row < cn;
+                wp[i] = reinterpret_cast<const uint4 *>(p2 + (size_t)(r0 + ch0 + (ok[i] ? row : rr)) * p.r);
+            }
+            float acc[RW][NB];
 #pragma unroll
             for (int i = 0; i < RW; ++i)
 #pragma unroll
+                for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
+            for (int c0 = lane; c0 < nch; c0 += 32 * 4) {
+                uint4 v[RW][4];
+#pragma unroll
+                for (int i = 0; i < RW; ++i)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int cc = c0 + 32 * u;
+                        if (ok[i] && cc < nch) v[i][u] = ld_stream(wp[i] + cc);
+                    }
+#pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int c = c0 + 32 * u;
-                    if (ok[i] && c < nch) v[i][u] = ld_stream(wp[i] + c);
+                    const int cc = c0 + 32 * u;
+                    if (cc < nch) {
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            if (b < p.B) {
+                                const float *hb = hs + (size_t)b * p.r + cc * EPC;
+#pragma unroll
+                                for (int i = 0; i < RW; ++i)
+                                    if (ok[i]) acc[i][b] += dot_chunk<PT>(v[i][u], hb);
+                            }
+                        }
+                    }
                 }
+            }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + 32 * u;
-                if (c < nch) {
+            for (int i = 0; i < RW; ++i) {
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        if (b < p.B) {
-                            const float *hb = hs + (size_t)b * p.r + c * EPC;
-#pragma unroll
-                            for (int i = 0; i < RW; ++i)
-                                if (ok[i]) acc[i][b] += dot_chunk<PT>(v[i][u], hb);
+                for (int b = 0; b < NB; ++b) {
+                    if (b < p.B) {
+                        const float sum = warp_sum(acc[i][b]);
+                        const int row = rr + i * kLWarps;
+                        if (lane == 0 && ok[i]) {
+                            const float l = sum + pb[row];
+                            lg[b * kChunk + row] = l;
+                            if (p.logits) p.logits[(size_t)b * p.F + r0 + ch0 + row] = l;
                         }
                     }
                 }
             }
         }
+        __syncthreads();
+        // threshold + union -> this chunk's mask words
+        for (int wd = warp; wd < (cn + 31) / 32; wd += kLWarps) {
+            const int row = wd * 32 + lane;
+            bool on = false;
+            if (row < cn) {
 #pragma unroll
-        for (int i = 0; i < RW; ++i) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (b < p.B) {
-                    const float sum = warp_sum(acc[i][b]);
-                    const int row = rr + i * kWarps;
-                    if (lane == 0 && ok[i]) {
-                        const int j = tile_start + row;
-                        const float l = sum + pb[row];
-                        lg[b * p.tile_rows + row] = l;
-                        if (p.logits) p.logits[(size_t)b * p.F + j] = l;
-                    }
-                }
+                for (int b = 0; b < NB; ++b)
+                    if (b < p.B) on = on || (lg[b * kChunk + row] > p.tau);
+                if (p.mask) p.mask[r0 + ch0 + row] = on ? 1 : 0;
             }
+            const unsigned bits = __ballot_sync(0xffffffffu, on);
+            if (lane == 0) words[ch0 / 32 + wd] = bits;
         }
+        __syncthreads();
     }
-    __syncthreads();
 
-    // threshold + union -> mask words
-    const int nw = (nrows + 31) >> 5;
-    for (int wd = warp; wd < nw; wd += kWarps) {
-        const int row = wd * 32 + lane;
-        bool on = false;
-        if (row < nrows) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                if (b < p.B) on = on || (lg[b * p.tile_rows + row] > p.tau);
-            if (p.mask) p.mask[tile_start + row] = on ? 1 : 0;
-        }
-        const unsigned bits = __ballot_sync(0xffffffffu, on);
-        if (lane == 0) sm.words[wd] = bits;
-    }
-    __syncthreads();
-    scan_emit(sm, p.ntiles, tile_start, nw, p.idx, p.n_active, p.cap, p.ctrl, p.status);
+    const unsigned epoch = s_epoch;
+    const unsigned count = scan_words<kLThreads>(words, wpre, nw, red);
+    const unsigned base = sum_before<kLThreads>(p.status, c, count, epoch, &p.ctrl->err, red);
+    write_total(c, G, base, count, p.n_active, p.cap, &p.ctrl->err);
+    emit_idx<kLThreads>(words, wpre, nw, r0, base, p.idx, p.cap);
 
     // Initialise the FFN output (b_down + residual) for the sparse kernel that
-    // follows: this tile's share of the B*d values.
+    // follows: this CTA's share of the B*d values.
     if (p.y) {
         const int nvec = p.B * p.d / 4;
-        const int v0 = (int)((long long)nvec * tile / p.ntiles);
-        const int v1 = (int)((long long)nvec * (tile + 1) / p.ntiles);
+        const int v0 = (int)((long long)nvec * c / G);
+        const int v1 = (int)((long long)nvec * (c + 1) / G);
         float4 *y4 = reinterpret_cast<float4 *>(p.y);
-        for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
+        for (int v = v0 + threadIdx.x; v < v1; v += kLThreads) {
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
             if (p.b_down) o = reinterpret_cast<const float4 *>(p.b_down)[v % (p.d / 4)];
             if (p.residual) {
@@ -358,32 +371,39 @@ __global__ void __launch_bounds__(kThreads) k_pred_logits(PredParams p)
             y4[v] = o;
         }
     }
-    scan_finish(p.ctrl, p.ntiles, sm.epoch);
+    scan_finish(p.ctrl, G, epoch);
 }
 
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_compact(const uint8_t *__restrict__ mask, int n, int *idx, int *count,
-                                                      int cap, WsCtrl *ctrl, unsigned long long *status, int ntiles,
-                                                      int tile_rows)
+constexpr int kCThreads = 256;
+
+__global__ void __launch_bounds__(kCThreads, 1) k_compact(const uint8_t *__restrict__ mask, int n, int *idx,
+                                                          int *count_out, int cap, WsCtrl *ctrl,
+                                                          unsigned long long *status)
 {
-    __shared__ ScanSmem sm;
+    extern __shared__ __align__(16) unsigned cw[];
+    __shared__ unsigned red[kCThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int r0 = (int)((long long)n * c / G);
+    const int R = (int)((long long)n * (c + 1) / G) - r0;
+    const int nw = (R + 31) >> 5;
+    unsigned *words = cw, *wpre = cw + nw;
     pdl_wait();
     pdl_trigger();
-    scan_start(sm, ctrl, ntiles);
-    __syncthreads();
-    const int tile_start = (int)sm.tile * tile_rows;
-    const int nrows = min(tile_rows, n - tile_start);
-    const int nw = (nrows + 31) >> 5;
-    for (int wd = warp; wd < nw; wd += kWarps) {
+    const unsigned epoch = *reinterpret_cast<volatile unsigned *>(&ctrl->epoch);
+    for (int wd = warp; wd < nw; wd += kCThreads / 32) {
         const int row = wd * 32 + lane;
-        const bool on = row < nrows && mask[tile_start + row] != 0;
+        const bool on = row < R && mask[r0 + row] != 0;
         const unsigned bits = __ballot_sync(0xffffffffu, on);
-        if (lane == 0) sm.words[wd] = bits;
+        if (lane == 0) words[wd] = bits;
     }
     __syncthreads();
-    scan_emit(sm, ntiles, tile_start, nw, idx, count, cap, ctrl, status);
-    scan_finish(ctrl, ntiles, sm.epoch);
+    const unsigned cnt = scan_words<kCThreads>(words, wpre, nw, red);
+    const unsigned base = sum_before<kCThreads>(status, c, cnt, epoch, &ctrl->err, red);
+    write_total(c, G, base, cnt, count_out, cap, &ctrl->err);
+    emit_idx<kCThreads>(words, wpre, nw, r0, base, idx, cap);
+    scan_finish(ctrl, G, epoch);
 }
 
 }  // namespace
@@ -407,10 +427,16 @@ cudaError_t launch_pred_hidden(int ptype, const void *p1, const float *x, int B,
                       static_cast<const uint8_t *>(p2), p2_bytes, p_bias, b_act, F);
 }
 
+// One CTA per SM (never more CTAs than SMs, so all are resident together),
+// and never more CTAs than 32-neuron words.
+int scan_grid(int n) { return std::max(1, std::min(sm_count(), (n + 31) / 32)); }
+
 template <typename PT>
 static cudaError_t pred_logits_nb(const PredParams &p, cudaStream_t s)
 {
-    const size_t smem = ((size_t)p.B * p.r + (size_t)9 * p.tile_rows) * sizeof(float);
+    const int G = scan_grid(p.F);
+    const int nw = ((p.F + G - 1) / G + 31) / 32 + 1;
+    const size_t smem = ((size_t)p.B * p.r + (size_t)9 * kChunk) * sizeof(float) + (size_t)2 * nw * sizeof(unsigned);
     void (*k)(PredParams);
     if (p.B <= 1)
         k = k_pred_logits<PT, 1>;
@@ -420,8 +446,9 @@ static cudaError_t pred_logits_nb(const PredParams &p, cudaStream_t s)
         k = k_pred_logits<PT, 4>;
     else
         k = k_pred_logits<PT, 8>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return launch_pdl(k, dim3(p.ntiles), dim3(kThreads), smem, s, p);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, dim3(G), dim3(kLThreads), smem, s, p);
 }
 
 cudaError_t launch_pred_logits(int ptype, const PredParams &p, cudaStream_t s)
@@ -432,9 +459,12 @@ cudaError_t launch_pred_logits(int ptype, const PredParams &p, cudaStream_t s)
 cudaError_t launch_compact(const uint8_t *mask, int n, int *idx, int *count, int cap, WsCtrl *ctrl,
                            unsigned long long *status, cudaStream_t s)
 {
-    const ScanGeom g = scan_geom(n);
-    return launch_pdl(k_compact, dim3(g.ntiles), dim3(kThreads), 0, s, mask, n, idx, count, cap, ctrl, status,
-                      g.ntiles, g.tile_rows);
+    const int G = scan_grid(n);
+    const int nw = ((n + G - 1) / G + 31) / 32 + 1;
+    const size_t smem = (size_t)2 * nw * sizeof(unsigned);
+    cudaError_t e = cudaFuncSetAttribute(k_compact, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_compact, dim3(G), dim3(kCThreads), smem, s, mask, n, idx, count, cap, ctrl, status);
 }
 
 }  // namespace pi

@@ -99,8 +99,9 @@ typedef void *pi_stream; /* cudaStream_t */
  *   b_act [d_ff], b_down [d_model], p_bias [d_ff]: fp32, 4-byte aligned, may
  *     each be NULL (= zero).  w_gate is NULL unless gated.
  * Limits: 8 <= d_model <= PI_MAX_D_MODEL and d_model % 8 == 0 (% 256 for
- *   Q4_0); 1 <= d_ff < 2^26; 8 <= rank <= PI_MAX_RANK, rank % 8 == 0 (only
- *   checked by calls that run the predictor).
+ *   Q4_0); 1 <= d_ff < 2^26 (< 2^23 for calls that run the predictor);
+ *   8 <= rank <= PI_MAX_RANK, rank % 8 == 0 (only checked by calls that run
+ *   the predictor).
  */
 typedef struct {
     int32_t d_model;
