@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "PI_OK", 1: "PI_ERR_NULL", 2: "PI_ERR_SHAPE", 3: "PI_ERR_DTYP
 # every symbol include/pi.h declares
 EXPORTS = ("pi_status_str", "pi_workspace_bytes", "pi_compact_workspace_bytes", "pi_compact", "pi_predict",
            "pi_sparse_ffn", "pi_ffn_layer", "pi_dense_ffn", "pi_q4_0_bytes", "pi_quantize_q4_0",
-           "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_rms_residual", "pi_sync_status")
+           "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_rms_residual", "pi_sync_status",
+           "pi_ffn_layer_static")
 
 
 class PiError(RuntimeError):
@@ -76,6 +77,7 @@ def lib():
             "pi_permute_rows": ([P, P, i64, i64, P, P], i32),
             "pi_rms_residual": ([P, P, i32, i32, P, P], i32),
             "pi_sync_status": ([P, sz, P], i32),
+            "pi_ffn_layer_static": ([D, P, P, P, P, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)

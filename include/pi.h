@@ -257,6 +257,32 @@ PI_API pi_status pi_rms_residual(const float *x, const float *y, int32_t batch, 
  */
 PI_API pi_status pi_sync_status(void *ws, size_t ws_bytes, pi_stream stream);
 
+/*
+ * pi_ffn_layer at batch 1 without a caller-provided workspace, for callers
+ * that cannot allocate device memory (code in a host callback or an allocator
+ * hook, plugins whose host forbids cudaMalloc, threads that must not risk the
+ * device-wide synchronisation cudaMalloc / cudaFree can cause).  This entry
+ * point is an engineering addition with no counterpart in the method's pages.
+ *
+ * Scratch space is a fixed file-scope device array of 320 KiB inside the
+ * library, present on every GPU that loads it until the process exits.  Limits:
+ * d_ff <= 65536 and rank <= PI_MAX_RANK; larger layers return PI_ERR_SHAPE.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Nothing is allocated by any call.
+ *
+ * All calls share the array and it keeps the last call's contents; each call
+ * clears its error word first.  Calls that overlap on the GPU (other streams
+ * or unordered host threads) race on it and give wrong results.
+ *   x, residual, y, idx, n_active: as in pi_ffn_layer with batch 1 (idx and
+ *   n_active may both be NULL).
+ *   status_out: device int32 [1] or NULL; receives the device error bits of
+ *   this call when it completes (0 = none; 1 = a bounded device wait gave up;
+ *   2 = active list over capacity; 4 = a neuron index out of range).
+ */
+PI_API pi_status pi_ffn_layer_static(const pi_ffn_desc *desc, const float *x, const float *residual, float *y,
+                                     int32_t *idx, int32_t *n_active, int32_t *status_out, pi_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
