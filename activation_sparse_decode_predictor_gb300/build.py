@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpi_sparse_ffn.so")
-SOURCES = ["api.cu", "predict.cu", "sparse_ffn.cu", "union_mma.cu", "aux.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "predict.cu", "sparse_ffn.cu", "layer_fused.cu", "union_mma.cu", "aux.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

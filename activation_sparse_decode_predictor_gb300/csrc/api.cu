@@ -19,8 +19,8 @@ WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
     size_t o = 0;
     L.ctrl = o;
     o += sizeof(WsCtrl);
-    L.status = o;
-    o = align256(o + (size_t)((d_ff + 31) / 32) * 8);
+    L.status = o;  // scan status words; also the two flag arrays of the fused layer kernel
+    o = align256(o + (size_t)std::max((d_ff + 31) / 32, 2 * kFusedMaxG) * 8);
     L.h = o;
     o = align256(o + (size_t)batch * (size_t)rank * 4);
     L.idx = o;
@@ -256,11 +256,20 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
     const WsLayout L = ws_layout(desc->d_model, desc->d_ff, desc->rank, batch);
     st = check_ws(ws, ws_bytes, L.total);
     if (st != PI_OK) return st;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (batch == 1 && fused_layer_supported(desc->wtype, desc->ptype, desc->d_model, desc->d_ff, desc->rank)) {
+        // one kernel per token: predictor, scan and sparse FFN without kernel boundaries
+        return cuda_status(launch_layer_b1(desc->wtype, desc->ptype, desc->gated, desc->act, desc->p1, desc->p2,
+                                           desc->p_bias, desc->threshold, desc->rank, desc->w_up, desc->w_gate,
+                                           desc->w_down, desc->b_act, desc->b_down, x, residual, y, idx, n_active,
+                                           at<int32_t>(ws, L.idx), at<float>(ws, L.h),
+                                           at<unsigned long long>(ws, L.status), at<WsCtrl>(ws, L.ctrl),
+                                           desc->d_model, desc->d_ff, s));
+    }
     if (!idx) {
         idx = at<int32_t>(ws, L.idx);
         n_active = at<int32_t>(ws, L.nact);
     }
-    const cudaStream_t s = (cudaStream_t)stream;
     st = enqueue_predict(desc, x, batch, nullptr, nullptr, idx, n_active, desc->d_ff, ws, y, residual, s);
     if (st != PI_OK) return st;
     return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s);

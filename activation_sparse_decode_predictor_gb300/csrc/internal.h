@@ -88,6 +88,15 @@ struct SparseParams {
 cudaError_t launch_sparse_b1(int wtype, int gated, const SparseParams &p, cudaStream_t s);
 cudaError_t launch_sparse_union(int wtype, int gated, const SparseParams &p, cudaStream_t s);
 
+// ---- one token through one layer in one kernel (layer_fused.cu) -------------------
+constexpr int kFusedMaxG = 1024;  // status words per flag array
+bool fused_layer_supported(int wtype, int ptype, int d, int F, int r);
+cudaError_t launch_layer_b1(int wtype, int ptype, int gated, int act, const void *p1, const void *p2,
+                            const float *p_bias, float tau, int r, const void *w_up, const void *w_gate,
+                            const void *w_down, const float *b_act, const float *b_down, const float *x,
+                            const float *residual, float *y, int *idx_out, int *n_active, int *cand, float *h,
+                            unsigned long long *flags, WsCtrl *ctrl, int d, int F, cudaStream_t s);
+
 // ---- small kernels (aux.cu) ------------------------------------------------------
 cudaError_t launch_init_y(float *y, const float *b_down, const float *residual, int B, int d,
                           int *iota_idx, int *iota_n, int iota_count, cudaStream_t s);

@@ -1,0 +1,640 @@
+// One decode token through one FFN layer in a single kernel (batch 1): the
+// predictor, the active-neuron scan and the neuron-aware sparse FFN, without
+// kernel boundaries between them.
+//
+// Method (PowerInfer summary page, "核心创新" core innovation and "方法详解"
+// method detail): an online predictor marks the neurons expected to fire and
+// neuron-aware sparse operators compute only those neurons.  Predictor form,
+// as in predict.cu: h = max(P1 x, 0), logit = P2 h + p_bias, active when
+// logit > threshold.  FFN as in sparse_ffn.cu.
+//
+// GB300 design.  One CTA per SM (all CTAs resident together), 1 producer warp
+// + 8 consumer warps.  The producer thread streams every byte the CTA needs
+// through one ring of shared-memory stages with 1-D bulk copies completing on
+// mbarriers, in job order:
+//   P1 rows      this CTA's share of the predictor's first matrix,
+//   P2 groups    8 rows of P2 each, for this CTA's contiguous neuron range,
+//   FFN jobs     up/gate rows of this CTA's share of the active neurons, and
+//                the down row of each neuron whose activation is non-zero.
+// The P1 and P2 jobs do not depend on the previous kernel, so they are issued
+// before the programmatic-dependent-launch wait and overlap the previous
+// kernel.  The consumers:
+//   1. compute their P1 rows (CTA reductions) -> h slice -> global, publish a
+//      flag; wait for every CTA's flag (barrier A) and load all of h;
+//   2. compute the logits of their neuron range, threshold, ballot, write the
+//      range's active neurons to a candidate list, publish the count; read all
+//      counts (barrier B): the prefix gives this range's place in the
+//      ascending active list and the total n;
+//   3. take the balanced share [n*c/G, n*(c+1)/G) of the global active list,
+//      look each entry up in the candidate lists, and hand the producer the
+//      neuron ids (an mbarrier); then run the FFN jobs as sparse_ffn.cu does,
+//      and add the CTA's partial output to y with 16-byte vector atomics.
+// Flags and counts carry the launch's epoch; CTA 0 moves the epoch on once
+// every CTA has published its count.  Every wait is bounded.
+#include <algorithm>
+
+#include "ffn_rows.cuh"
+#include "internal.h"
+
+namespace pi {
+
+namespace {
+
+constexpr int kNCW = 8;
+constexpr int kNCT = kNCW * 32;
+constexpr int kThreads = kNCT + 32;
+constexpr int kMaxStages = 16;
+constexpr int kMaxShare = 512;     // FFN rows per CTA (share of the active list)
+constexpr int kMaxRange = 512;     // neurons per CTA range (P2 rows)
+constexpr int kMaxG = 1024;
+constexpr int kMaxRank = 2048;
+constexpr int kGroup = 8;          // P2 rows per job
+constexpr int kJobP1 = 1, kJobP2 = 2, kJobUp = 3, kJobDown = 4, kJobEnd = 5;
+
+struct Tables {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t share_ready;
+    int4 job[kMaxStages];
+    float red[2][kNCW][2];
+    unsigned epoch;
+    int share_n;
+    int count, total;
+    int wsum[kNCW];
+    unsigned words[kMaxRange / 32 + 1];
+    unsigned wpre[kMaxRange / 32 + 1];
+    float lg[kMaxRange];
+    float pb[kMaxRange];
+    float hs[kMaxRank];
+    int pref[kMaxG];
+    int j[kMaxShare];
+    float bias[kMaxShare];
+    float a[kMaxShare];
+    int state[kMaxShare];
+};
+constexpr size_t kHdr = (sizeof(Tables) + 1023) & ~(size_t)1023;
+
+__device__ __forceinline__ unsigned long long tagged(unsigned epoch, unsigned v)
+{
+    return ((unsigned long long)(((epoch & 0x7fffffffu) << 1) | 1u) << 32) | v;
+}
+
+__device__ __forceinline__ unsigned tag_of(unsigned epoch) { return ((epoch & 0x7fffffffu) << 1) | 1u; }
+
+__device__ __forceinline__ int ld_cg_int(const int *p)
+{
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// Bounded wait of one thread for a tagged word of this epoch; returns its value.
+__device__ __forceinline__ unsigned wait_tagged(const unsigned long long *w, unsigned epoch, unsigned *err,
+                                                bool *ok)
+{
+    const unsigned want = tag_of(epoch);
+    for (long long i = 0; i < kSpinLimit; ++i) {
+        const unsigned long long s = ld_volatile_u64(w);
+        if ((unsigned)(s >> 32) == want) return (unsigned)s;
+    }
+    atomicOr(err, ERR_TIMEOUT);
+    *ok = false;
+    return 0u;
+}
+
+template <typename PT>
+__device__ __forceinline__ float dot16(uint4 w, const float *x);
+template <>
+__device__ __forceinline__ float dot16<__half>(uint4 w, const float *x) { return dot8_f16(w, x); }
+template <>
+__device__ __forceinline__ float dot16<float>(uint4 w, const float *x) { return dot4_f32(w, x); }
+
+struct FusedParams {
+    const uint8_t *p1, *p2;
+    const float *p_bias;
+    const uint8_t *w_act, *w_up, *w_down;
+    const float *b_act, *b_down;
+    const float *x, *residual;
+    float *y;
+    int *idx_out;        // ordered active list, or null
+    int *n_active;       // or null
+    int *cand;           // [F] candidate lists (each CTA writes inside its range)
+    float *h;            // [rank]
+    unsigned long long *flag_h, *status;  // [G] each
+    WsCtrl *ctrl;
+    int d, F, r, act;
+    float tau;
+};
+
+template <int WT, typename PT, bool GATED, int CH>
+__global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
+{
+    constexpr int EPC = Fmt<WT>::EPC;                // weight elements per 16-byte chunk
+    constexpr int PSEG = EPC * (int)sizeof(PT) / 16; // P1 chunks covering one weight chunk's columns
+    constexpr int PEPC = 16 / (int)sizeof(PT);       // predictor elements per 16-byte chunk
+    static_assert(PSEG >= 1, "predictor chunk wider than a weight chunk");
+    extern __shared__ __align__(128) uint8_t smem[];
+    Tables &T = *reinterpret_cast<Tables *>(smem);
+    uint8_t *stages = smem + kHdr;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int d = p.d, F = p.F, r = p.r;
+    const uint32_t R = row_slot_bytes(WT, d);
+    const int nch = d / EPC;
+    unsigned *err = &p.ctrl->err;
+    const int hk0 = (int)((long long)r * c / G), hk1 = (int)((long long)r * (c + 1) / G);
+    const int j0 = (int)((long long)F * c / G), j1 = (int)((long long)F * (c + 1) / G);
+    const int nP1 = hk1 - hk0, nR = j1 - j0;
+    const int nP2 = (nR + kGroup - 1) / kGroup;
+    const uint32_t p1row = (uint32_t)d * sizeof(PT), p2row = (uint32_t)r * sizeof(PT);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nstages; ++s) {
+            mbar_init(&T.full[s], 1);
+            mbar_init(&T.empty[s], kNCW);
+        }
+        mbar_init(&T.share_ready, 1);
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < kMaxShare; i += kThreads) T.state[i] = 0;
+    for (int i = threadIdx.x; i < nR; i += kThreads) T.pb[i] = p.p_bias ? p.p_bias[j0 + i] : 0.f;
+    __syncthreads();
+
+    if (warp == kNCW) {
+        // ================================ producer =================================
+        int q = 0;
+        bool failed = false;
+        if (lane == 0) {
+            auto acquire = [&](int qq) -> bool {
+                const int s = qq % nstages;
+                return qq < nstages || mbar_wait(&T.empty[s], (unsigned)((qq / nstages) - 1) & 1u, err);
+            };
+            // predictor jobs: independent of the previous kernel, issued at once
+            for (int i = 0; i < nP1 + nP2 && !failed; ++i) {
+                if (!acquire(q)) {
+                    failed = true;
+                    break;
+                }
+                const int s = q % nstages;
+                uint8_t *st = stages + (size_t)s * stage_bytes;
+                if (i < nP1) {
+                    T.job[s] = make_int4(kJobP1, hk0 + i, 0, 0);
+                    mbar_arrive_expect_tx(&T.full[s], p1row);
+                    bulk_g2s(st, p.p1 + (size_t)(hk0 + i) * p1row, p1row, &T.full[s]);
+                } else {
+                    const int g0 = j0 + (i - nP1) * kGroup, g1 = min(g0 + kGroup, j1);
+                    const uint32_t bytes = (uint32_t)(g1 - g0) * p2row;
+                    T.job[s] = make_int4(kJobP2, g0, g1, 0);
+                    mbar_arrive_expect_tx(&T.full[s], bytes);
+                    bulk_g2s(st, p.p2 + (size_t)g0 * p2row, bytes, &T.full[s]);
+                }
+                ++q;
+            }
+            // FFN jobs, once the consumers have found this CTA's share
+            if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
+            const int sn = failed ? 0 : T.share_n;
+            volatile int *state = T.state;
+            int up = 0, ds = 0;
+            while (!failed) {
+                int kind, i = 0, j = 0;
+                if (ds < up && state[ds] != 0) {
+                    const int stt = state[ds];
+                    i = ds++;
+                    if (stt == 1) continue;
+                    kind = kJobDown;
+                    j = T.j[i];
+                } else if (up < sn) {
+                    i = up++;
+                    j = T.j[i];
+                    if (j < 0 || j >= F) {
+                        atomicOr(err, ERR_INDEX);
+                        T.a[i] = 0.f;
+                        state[i] = 1;
+                        continue;
+                    }
+                    kind = kJobUp;
+                } else if (ds < sn) {
+                    long long spins = 0;
+                    while (state[ds] == 0 && ++spins < kSpinLimit) {
+                    }
+                    if (state[ds] == 0) {
+                        atomicOr(err, ERR_TIMEOUT);
+                        failed = true;
+                        kind = kJobEnd;
+                    } else {
+                        continue;
+                    }
+                } else {
+                    kind = kJobEnd;
+                }
+                if (!acquire(q)) {
+                    failed = true;
+                    break;
+                }
+                const int s = q % nstages;
+                uint8_t *st = stages + (size_t)s * stage_bytes;
+                T.job[s] = make_int4(kind, i, j, 0);
+                if (kind == kJobUp) {
+                    mbar_arrive_expect_tx(&T.full[s], GATED ? 2u * R : R);
+                    copy_row<WT>(st, p.w_act, j, d, F, &T.full[s]);
+                    if constexpr (GATED) copy_row<WT>(st + R, p.w_up, j, d, F, &T.full[s]);
+                } else if (kind == kJobDown) {
+                    mbar_arrive_expect_tx(&T.full[s], R);
+                    copy_row<WT>(st, p.w_down, j, d, F, &T.full[s]);
+                } else {
+                    mbar_arrive(&T.full[s]);
+                }
+                ++q;
+                if (kind == kJobEnd) break;
+            }
+            if (failed) {
+                for (int s = 0; s < nstages && s < q; ++s) {
+                    const int last = s + ((q - 1 - s) / nstages) * nstages;
+                    mbar_wait(&T.full[s], (unsigned)(last / nstages) & 1u, err);
+                }
+            }
+        }
+        return;
+    }
+
+    // ================================= consumers ===================================
+    const int t = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (t == 0) T.epoch = *reinterpret_cast<volatile unsigned *>(&p.ctrl->epoch);
+
+    // y = b_down + residual, this CTA's share; made visible before the flag below
+    {
+        const int nvec = d / 4;
+        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
+        for (int v = v0 + t; v < v1; v += kNCT) {
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p.b_down) o = reinterpret_cast<const float4 *>(p.b_down)[v];
+            if (p.residual) {
+                const float4 rz = reinterpret_cast<const float4 *>(p.residual)[v];
+                o.x += rz.x;
+                o.y += rz.y;
+                o.z += rz.z;
+                o.w += rz.w;
+            }
+            reinterpret_cast<float4 *>(p.y)[v] = o;
+        }
+        __threadfence();
+    }
+
+    float xr[CH][EPC];
+    float acc[CH][EPC];
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+        const int cc = t + kNCT * u;
+#pragma unroll
+        for (int e = 0; e < EPC; e += 4) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (cc < nch) v = *reinterpret_cast<const float4 *>(p.x + (size_t)cc * EPC + e);
+            xr[u][e] = v.x;
+            xr[u][e + 1] = v.y;
+            xr[u][e + 2] = v.z;
+            xr[u][e + 3] = v.w;
+            acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
+        }
+    }
+    named_bar_sync(1, kNCT);
+    const unsigned epoch = T.epoch;
+    bool ok = true;
+    int q = 0, ub = 0;
+
+    auto release = [&](int s) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&T.empty[s]);
+    };
+
+    // ---- 1. hidden layer: this CTA's P1 rows ----
+    for (int i = 0; i < nP1 && ok; ++i, ++q) {
+        const int s = q % nstages;
+        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
+            ok = false;
+            break;
+        }
+        const uint8_t *st = stages + (size_t)s * stage_bytes;
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+            const int cc = t + kNCT * u;
+            if (cc < nch) {
+#pragma unroll
+                for (int g = 0; g < PSEG; ++g)
+                    part += dot16<PT>(*reinterpret_cast<const uint4 *>(st + ((size_t)cc * PSEG + g) * 16),
+                                      &xr[u][g * PEPC]);
+            }
+        }
+        part = warp_sum(part);
+        if (lane == 0) T.red[ub & 1][warp][0] = part;
+        named_bar_sync(1, kNCT);
+        if (t == 0) {
+            float z = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNCW; ++w) z += T.red[ub & 1][w][0];
+            p.h[T.job[s].y] = fmaxf(z, 0.f);
+        }
+        ++ub;
+        release(s);
+    }
+    if (t == 0) {
+        __threadfence();
+        st_volatile_u64(&p.flag_h[c], tagged(epoch, 1u));
+    }
+    // barrier A: every CTA's h slice (and y initialisation) is out
+    for (int i = t; i < G; i += kNCT) {
+        bool o2 = true;
+        wait_tagged(&p.flag_h[i], epoch, err, &o2);
+        ok = ok && o2;
+    }
+    named_bar_sync(1, kNCT);
+    for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
+    named_bar_sync(1, kNCT);
+
+    // ---- 2. logits of this CTA's neuron range ----
+    for (int i = 0; i < nP2 && ok; ++i, ++q) {
+        const int s = q % nstages;
+        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
+            ok = false;
+            break;
+        }
+        const uint8_t *st = stages + (size_t)s * stage_bytes;
+        const int4 job = T.job[s];
+        const int row = job.y + warp;  // one row per consumer warp
+        if (row < job.z) {
+            const uint8_t *pr = st + (size_t)warp * p2row;
+            float sum = 0.f;
+            for (int cc = lane; cc < r / PEPC; cc += 32)
+                sum += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
+            sum = warp_sum(sum);
+            if (lane == 0) T.lg[row - j0] = sum + T.pb[row - j0];
+        }
+        release(s);
+    }
+    named_bar_sync(1, kNCT);
+    const int nw = (nR + 31) >> 5;
+    for (int wd = warp; wd < nw; wd += kNCW) {
+        const int row = wd * 32 + lane;
+        const bool on = row < nR && T.lg[row] > p.tau;
+        const unsigned bits = __ballot_sync(0xffffffffu, on);
+        if (lane == 0) T.words[wd] = bits;
+    }
+    named_bar_sync(1, kNCT);
+    if (t == 0) {
+        int run = 0;
+        for (int wd = 0; wd < nw; ++wd) {
+            T.wpre[wd] = run;
+            run += __popc(T.words[wd]);
+        }
+        T.count = run;
+    }
+    named_bar_sync(1, kNCT);
+    // candidate list of this range: ascending active neurons, at cand[j0 ...)
+    for (int wd = warp; wd < nw; wd += kNCW) {
+        const unsigned bits = T.words[wd];
+        if ((bits >> lane) & 1u) p.cand[j0 + T.wpre[wd] + __popc(bits & ((1u << lane) - 1u))] = j0 + wd * 32 + lane;
+    }
+    __threadfence();
+    named_bar_sync(1, kNCT);
+    if (t == 0) st_volatile_u64(&p.status[c], tagged(epoch, (unsigned)T.count));
+
+    // barrier B: every range's count -> exclusive prefix and total
+    for (int i = t; i < G; i += kNCT) {
+        bool o2 = true;
+        T.pref[i] = (int)wait_tagged(&p.status[i], epoch, err, &o2);
+        ok = ok && o2;
+    }
+    named_bar_sync(1, kNCT);
+    {   // exclusive scan of the G counts by the consumer threads
+        const int per = (G + kNCT - 1) / kNCT;
+        const int i0 = min(G, t * per), i1 = min(G, i0 + per);
+        int mine = 0;
+        for (int i = i0; i < i1; ++i) mine += T.pref[i];
+        int inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        if (lane == 31) T.wsum[warp] = inc;
+        named_bar_sync(1, kNCT);
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kNCW; ++w) {
+            if (w < warp) before += T.wsum[w];
+            total += T.wsum[w];
+        }
+        int run = before + inc - mine;
+        for (int i = i0; i < i1; ++i) {
+            const int v = T.pref[i];
+            T.pref[i] = run;
+            run += v;
+        }
+        if (t == 0) {
+            T.total = total;
+            if (c == 0) atomicExch(&p.ctrl->epoch, epoch + 1u);  // every CTA has read this launch's epoch
+            if (c == G - 1 && p.n_active) *p.n_active = total;
+        }
+    }
+    named_bar_sync(1, kNCT);
+    const int n = T.total;
+    if (p.idx_out) {  // this range's part of the ordered active list
+        for (int i = t; i < T.count; i += kNCT) p.idx_out[T.pref[c] + i] = p.cand[j0 + i];
+    }
+    // this CTA's balanced share of the active list
+    const int k0 = (int)((long long)n * c / G), k1 = (int)((long long)n * (c + 1) / G);
+    const int sn = min(k1 - k0, kMaxShare);
+    for (int i = t; i < sn; i += kNCT) {
+        const int k = k0 + i;
+        int lo = 0, hi = G - 1;  // last range whose prefix <= k
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (T.pref[mid] <= k) lo = mid; else hi = mid - 1;
+        }
+        const int rs = (int)((long long)F * lo / G);
+        const int jn = ld_cg_int(p.cand + rs + (k - T.pref[lo]));
+        T.j[i] = jn;
+        T.bias[i] = (p.b_act && jn >= 0 && jn < F) ? p.b_act[jn] : 0.f;
+    }
+    named_bar_sync(1, kNCT);
+    if (t == 0) {
+        T.share_n = ok ? sn : 0;
+        mbar_arrive(&T.share_ready);
+    }
+
+    // ---- 3. the sparse FFN over this CTA's share ----
+    bool any = false;
+    while (ok) {
+        const int s = q % nstages;
+        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) break;
+        const int4 job = T.job[s];
+        if (job.x == kJobEnd) {
+            release(s);
+            ++q;
+            break;
+        }
+        const uint8_t *st = stages + (size_t)s * stage_bytes;
+        if (job.x == kJobUp) {
+            float pa = 0.f, pu = 0.f;
+#pragma unroll
+            for (int u = 0; u < CH; ++u) {
+                const int cc = t + kNCT * u;
+                if (cc < nch) {
+                    pa += chunk_dot<WT>(st, cc, d, xr[u]);
+                    if constexpr (GATED) pu += chunk_dot<WT>(st + R, cc, d, xr[u]);
+                }
+            }
+            pa = warp_sum(pa);
+            if constexpr (GATED) pu = warp_sum(pu);
+            if (lane == 0) {
+                T.red[ub & 1][warp][0] = pa;
+                T.red[ub & 1][warp][1] = pu;
+            }
+            named_bar_sync(1, kNCT);
+            if (t == 0) {
+                float z = 0.f, uu = 0.f;
+#pragma unroll
+                for (int w = 0; w < kNCW; ++w) {
+                    z += T.red[ub & 1][w][0];
+                    uu += T.red[ub & 1][w][1];
+                }
+                float a = activate(p.act, z + T.bias[job.y]);
+                if constexpr (GATED) a *= uu;
+                T.a[job.y] = a;
+                __threadfence_block();
+                *reinterpret_cast<volatile int *>(&T.state[job.y]) = (a != 0.f) ? 2 : 1;
+            }
+            ++ub;
+        } else {
+            const float a = T.a[job.y];
+#pragma unroll
+            for (int u = 0; u < CH; ++u) {
+                const int cc = t + kNCT * u;
+                if (cc < nch) chunk_axpy<WT>(st, cc, d, a, acc[u]);
+            }
+            any = true;
+        }
+        release(s);
+        ++q;
+    }
+    if (!any) return;
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+        const int cc = t + kNCT * u;
+        if (cc < nch) {
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4)
+                atomicAdd(reinterpret_cast<float4 *>(p.y + (size_t)cc * EPC + e),
+                          make_float4(acc[u][e], acc[u][e + 1], acc[u][e + 2], acc[u][e + 3]));
+        }
+    }
+}
+
+#ifndef PI_FUSED_SMEM_KB
+#define PI_FUSED_SMEM_KB 110
+#endif
+// Shared-memory budget of one CTA: small enough that the next layer's CTA can
+// start its predictor prefetch on the same SM while this one finishes.
+constexpr size_t g_smem_budget = (size_t)PI_FUSED_SMEM_KB * 1024;
+
+template <int WT, typename PT, bool GATED, int CH>
+cudaError_t launch_t(const FusedParams &p, int G, int ns, uint32_t stage_bytes, cudaStream_t s)
+{
+    auto k = k_layer_b1<WT, PT, GATED, CH>;
+    const size_t smem = kHdr + (size_t)ns * stage_bytes;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, dim3(G), dim3(kThreads), smem, s, p, ns, stage_bytes);
+}
+
+template <int WT, typename PT, bool GATED>
+cudaError_t launch_ch(const FusedParams &p, int need, int G, int ns, uint32_t sb, cudaStream_t s)
+{
+    if (need <= 1) return launch_t<WT, PT, GATED, 1>(p, G, ns, sb, s);
+    if (need <= 2) return launch_t<WT, PT, GATED, 2>(p, G, ns, sb, s);
+    if constexpr (WT != 2) {
+        if (need <= 3) return launch_t<WT, PT, GATED, 3>(p, G, ns, sb, s);
+        if (need <= 4) return launch_t<WT, PT, GATED, 4>(p, G, ns, sb, s);
+        if (need <= 6) return launch_t<WT, PT, GATED, 6>(p, G, ns, sb, s);
+        if (need <= 8) return launch_t<WT, PT, GATED, 8>(p, G, ns, sb, s);
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+bool fused_layer_supported(int wtype, int ptype, int d, int F, int r)
+{
+    const int G = sm_count();
+    if (G > kMaxG || r > kMaxRank) return false;
+    if (!((wtype == 1 && ptype == 1) || (wtype == 2 && ptype == 1) || (wtype == 0 && ptype == 0))) return false;
+    if ((F + G - 1) / G > kMaxRange) return false;
+    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
+    const int need = (d / epc + kNCT - 1) / kNCT;
+    return need <= (wtype == 2 ? 2 : 8);
+}
+
+cudaError_t launch_layer_b1(int wtype, int ptype, int gated, int act, const void *p1, const void *p2,
+                            const float *p_bias, float tau, int r, const void *w_up, const void *w_gate,
+                            const void *w_down, const float *b_act, const float *b_down, const float *x,
+                            const float *residual, float *y, int *idx_out, int *n_active, int *cand, float *h,
+                            unsigned long long *flags, WsCtrl *ctrl, int d, int F, cudaStream_t s)
+{
+    const int G = sm_count();
+    FusedParams p{};
+    p.p1 = static_cast<const uint8_t *>(p1);
+    p.p2 = static_cast<const uint8_t *>(p2);
+    p.p_bias = p_bias;
+    p.w_act = static_cast<const uint8_t *>(gated ? w_gate : w_up);
+    p.w_up = static_cast<const uint8_t *>(gated ? w_up : nullptr);
+    p.w_down = static_cast<const uint8_t *>(w_down);
+    p.b_act = b_act;
+    p.b_down = b_down;
+    p.x = x;
+    p.residual = residual;
+    p.y = y;
+    p.idx_out = idx_out;
+    p.n_active = n_active;
+    p.cand = cand;
+    p.h = h;
+    p.flag_h = flags;
+    p.status = flags + kMaxG;
+    p.ctrl = ctrl;
+    p.d = d;
+    p.F = F;
+    p.r = r;
+    p.act = act;
+    p.tau = tau;
+    const int esz = ptype == 1 ? 2 : 4;
+    const uint32_t R = row_slot_bytes(wtype, d);
+    uint32_t sb = std::max<uint32_t>({(uint32_t)d * esz, (uint32_t)kGroup * r * esz, (gated ? 2u : 1u) * R});
+    sb = (sb + 127u) & ~127u;
+    int ns = (int)((g_smem_budget - kHdr) / sb);
+    ns = std::min(ns, kMaxStages);
+    if (ns < 2) {
+        ns = 2;  // wide rows: accept a larger footprint rather than fail
+    }
+    if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
+    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
+    const int need = (d / epc + kNCT - 1) / kNCT;
+    switch (wtype * 2 + (gated ? 1 : 0)) {
+    case 0: return launch_ch<0, float, false>(p, need, G, ns, sb, s);
+    case 1: return launch_ch<0, float, true>(p, need, G, ns, sb, s);
+    case 2: return launch_ch<1, __half, false>(p, need, G, ns, sb, s);
+    case 3: return launch_ch<1, __half, true>(p, need, G, ns, sb, s);
+    case 4: return launch_ch<2, __half, false>(p, need, G, ns, sb, s);
+    case 5: return launch_ch<2, __half, true>(p, need, G, ns, sb, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pi

@@ -290,3 +290,28 @@ def test_fire_counts_and_hot_first_permutation():
     slack = (np.abs(z) <= 1e-4).sum(0)
     assert np.all(np.abs(got - ref) <= slack)
     assert np.array_equal(B.pi_hot_first_perm(ref), oracle.hot_first_perm(ref))
+
+
+@pytest.mark.parametrize("shape", [(256, 100, 8), (256, 151, 16), (512, 153, 2048 // 8), (1024, 77000, 64)])
+def test_ffn_layer_degenerate_ranges(shape):
+    """Layers with fewer neurons or predictor rows than SMs (empty per-CTA
+    ranges), and one too wide for the one-kernel path (the three-kernel
+    fallback): same parity criteria as test_ffn_layer_parity."""
+    d, F, r = shape
+    lay, olay, H = _layer(d, F, r, False, "f16", seed=F + r)
+    X = synth.tokens(2, d, 14).numpy()
+    ws = None
+    for t in range(2):
+        h, logit_ref, M = oracle.predict(olay, X[t])
+        amb = ambiguous(logit_ref, logit_scale(H, h), olay.threshold)
+        y = torch.empty(d, dtype=torch.float32, device="cuda")
+        idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = B.pi_ffn_layer(lay, _cuda(X[t]), y, idx=idx, n_active=n, ws=ws)
+        assert B.pi_sync_status(ws) == 0
+        got = set(idx.cpu().numpy()[: int(n.item())].tolist())
+        ref = set(np.flatnonzero(M).tolist())
+        assert all(amb[j] for j in got ^ ref)
+        idx_res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))),
+                           dtype=np.int32)
+        assert_ffn_close(y.cpu().numpy(), oracle.sparse_ffn(olay, X[t], idx_res), what=f"{shape} t={t}")
