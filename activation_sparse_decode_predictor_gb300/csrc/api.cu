@@ -19,14 +19,16 @@ WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
     size_t o = 0;
     L.ctrl = o;
     o += sizeof(WsCtrl);
-    L.status = o;  // scan status words; also the two flag arrays of the fused layer kernel
-    o = align256(o + (size_t)std::max((d_ff + 31) / 32, 2 * kFusedMaxG) * 8);
+    L.status = o;  // scan status words (the one-kernel layer step uses the first #SMs words)
+    o = align256(o + (size_t)std::max((d_ff + 31) / 32, 1024) * 8);
     L.h = o;
     o = align256(o + (size_t)batch * (size_t)rank * 4);
     L.idx = o;
     o = align256(o + (size_t)d_ff * 4);
     L.nact = o;
     o = align256(o + 16);
+    L.candb = o;
+    if (batch == 1) o = align256(o + (size_t)d_ff * 4);
     L.act = o;
     if (batch > 1) o = align256(o + (size_t)d_ff * 8 * 4);
     L.total = o;
@@ -259,12 +261,34 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
     const cudaStream_t s = (cudaStream_t)stream;
     if (batch == 1 && fused_layer_supported(desc->wtype, desc->ptype, desc->d_model, desc->d_ff, desc->rank)) {
         // one kernel per token: predictor, scan and sparse FFN without kernel boundaries
-        return cuda_status(launch_layer_b1(desc->wtype, desc->ptype, desc->gated, desc->act, desc->p1, desc->p2,
-                                           desc->p_bias, desc->threshold, desc->rank, desc->w_up, desc->w_gate,
-                                           desc->w_down, desc->b_act, desc->b_down, x, residual, y, idx, n_active,
-                                           at<int32_t>(ws, L.idx), at<float>(ws, L.h),
-                                           at<unsigned long long>(ws, L.status), at<WsCtrl>(ws, L.ctrl),
-                                           desc->d_model, desc->d_ff, s));
+        LayerB1Args a{};
+        a.wtype = desc->wtype;
+        a.ptype = desc->ptype;
+        a.gated = desc->gated;
+        a.act = desc->act;
+        a.p1 = desc->p1;
+        a.p2 = desc->p2;
+        a.p_bias = desc->p_bias;
+        a.tau = desc->threshold;
+        a.r = desc->rank;
+        a.w_up = desc->w_up;
+        a.w_gate = desc->w_gate;
+        a.w_down = desc->w_down;
+        a.b_act = desc->b_act;
+        a.b_down = desc->b_down;
+        a.x = x;
+        a.residual = residual;
+        a.y = y;
+        a.idx_out = idx;
+        a.n_active = n_active;
+        a.cand = at<int32_t>(ws, L.idx);
+        a.cand_bias = at<float>(ws, L.candb);
+        a.h = at<float>(ws, L.h);
+        a.status = at<unsigned>(ws, L.status);
+        a.ctrl = at<WsCtrl>(ws, L.ctrl);
+        a.d = desc->d_model;
+        a.F = desc->d_ff;
+        return cuda_status(launch_layer_b1(a, s));
     }
     if (!idx) {
         idx = at<int32_t>(ws, L.idx);

@@ -19,11 +19,13 @@ constexpr long long kSpinLimit = 1ll << 22;
 
 // First 256 bytes of a workspace.
 struct WsCtrl {
-    unsigned err;      // ERR_* bits, cleared by pi_sync_status
+    unsigned err;           // ERR_* bits, cleared by pi_sync_status
     unsigned spare;
-    unsigned done;     // scan: CTAs finished in the running launch
-    unsigned epoch;    // scan: launch generation, tags the CTA status words
-    unsigned pad[60];
+    unsigned done;          // scan: CTAs finished in the running launch
+    unsigned epoch;         // scan: launch generation, tags the CTA status words
+    unsigned bar_count[2];  // grid barriers of the one-kernel layer step: arrivals ...
+    unsigned bar_gen[2];    // ... and generation words
+    unsigned pad[56];
 };
 static_assert(sizeof(WsCtrl) == 256, "control block is 256 bytes");
 

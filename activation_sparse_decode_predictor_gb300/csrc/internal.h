@@ -17,6 +17,7 @@ struct WsLayout {
     size_t h;         // predictor hidden [batch][rank] fp32
     size_t idx;       // internal active list [d_ff] int32
     size_t nact;      // internal active count (int32)
+    size_t candb;     // one-kernel layer step: candidate biases [d_ff] fp32
     size_t act;       // union path: activations [d_ff][8] fp32
     size_t total;
 };
@@ -89,13 +90,26 @@ cudaError_t launch_sparse_b1(int wtype, int gated, const SparseParams &p, cudaSt
 cudaError_t launch_sparse_union(int wtype, int gated, const SparseParams &p, cudaStream_t s);
 
 // ---- one token through one layer in one kernel (layer_fused.cu) -------------------
-constexpr int kFusedMaxG = 1024;  // status words per flag array
+struct LayerB1Args {
+    int wtype, ptype, gated, act;
+    const void *p1, *p2;
+    const float *p_bias;
+    float tau;
+    int r;
+    const void *w_up, *w_gate, *w_down;
+    const float *b_act, *b_down;
+    const float *x, *residual;
+    float *y;
+    int *idx_out, *n_active;
+    int *cand;              // [F] workspace
+    float *cand_bias;       // [F] workspace
+    float *h;               // [r] workspace
+    unsigned *status;       // [#SMs] workspace
+    WsCtrl *ctrl;
+    int d, F;
+};
 bool fused_layer_supported(int wtype, int ptype, int d, int F, int r);
-cudaError_t launch_layer_b1(int wtype, int ptype, int gated, int act, const void *p1, const void *p2,
-                            const float *p_bias, float tau, int r, const void *w_up, const void *w_gate,
-                            const void *w_down, const float *b_act, const float *b_down, const float *x,
-                            const float *residual, float *y, int *idx_out, int *n_active, int *cand, float *h,
-                            unsigned long long *flags, WsCtrl *ctrl, int d, int F, cudaStream_t s);
+cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s);
 
 // ---- small kernels (aux.cu) ------------------------------------------------------
 cudaError_t launch_init_y(float *y, const float *b_down, const float *residual, int B, int d,

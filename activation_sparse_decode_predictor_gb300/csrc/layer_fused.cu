@@ -12,25 +12,27 @@
 // + 8 consumer warps.  The producer thread streams every byte the CTA needs
 // through one ring of shared-memory stages with 1-D bulk copies completing on
 // mbarriers, in job order:
-//   P1 rows      this CTA's share of the predictor's first matrix,
-//   P2 groups    8 rows of P2 each, for this CTA's contiguous neuron range,
+//   P1 jobs      consecutive rows of this CTA's share of the predictor's P1,
+//   P2 jobs      8 rows of P2 each, for this CTA's contiguous neuron range,
 //   FFN jobs     up/gate rows of this CTA's share of the active neurons, and
 //                the down row of each neuron whose activation is non-zero.
-// The P1 and P2 jobs do not depend on the previous kernel, so they are issued
-// before the programmatic-dependent-launch wait and overlap the previous
-// kernel.  The consumers:
-//   1. compute their P1 rows (CTA reductions) -> h slice -> global, publish a
-//      flag; wait for every CTA's flag (barrier A) and load all of h;
+// On entry, before the programmatic-dependent-launch wait, the producer asks
+// L2 for the CTA's whole predictor share (P1 and P2 do not depend on the
+// previous kernel) and fills the ring; later refills then come from L2.  The
+// consumers:
+//   1. compute their P1 rows -> h slice -> global; grid barrier A; load h;
 //   2. compute the logits of their neuron range, threshold, ballot, write the
-//      range's active neurons to a candidate list, publish the count; read all
-//      counts (barrier B): the prefix gives this range's place in the
-//      ascending active list and the total n;
-//   3. take the balanced share [n*c/G, n*(c+1)/G) of the global active list,
-//      look each entry up in the candidate lists, and hand the producer the
-//      neuron ids (an mbarrier); then run the FFN jobs as sparse_ffn.cu does,
-//      and add the CTA's partial output to y with 16-byte vector atomics.
-// Flags and counts carry the launch's epoch; CTA 0 moves the epoch on once
-// every CTA has published its count.  Every wait is bounded.
+//      range's active neurons (with their biases) to a candidate list and the
+//      count to a status word; grid barrier B; read all counts: the prefix
+//      gives this range's place in the ascending active list and the total n;
+//   3. take the balanced share [n*c/G, n*(c+1)/G) of the active list, look
+//      each entry up in the candidate lists and hand the neuron ids to the
+//      producer (an mbarrier), which asks L2 for all their rows at once and
+//      then runs the FFN jobs as sparse_ffn.cu does; the CTA's partial output
+//      goes to y with 16-byte vector atomics.
+// The grid barriers are counter barriers: one thread per CTA arrives with an
+// atomic add; the last arrival resets the counter and moves a generation word
+// on, which the other CTAs' single thread polls (bounded).
 #include <algorithm>
 
 #include "ffn_rows.cuh"
@@ -43,12 +45,13 @@ namespace {
 constexpr int kNCW = 8;
 constexpr int kNCT = kNCW * 32;
 constexpr int kThreads = kNCT + 32;
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 24;
 constexpr int kMaxShare = 512;     // FFN rows per CTA (share of the active list)
 constexpr int kMaxRange = 512;     // neurons per CTA range (P2 rows)
 constexpr int kMaxG = 1024;
 constexpr int kMaxRank = 2048;
 constexpr int kGroup = 8;          // P2 rows per job
+constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kJobP1 = 1, kJobP2 = 2, kJobUp = 3, kJobDown = 4, kJobEnd = 5;
 
 struct Tables {
@@ -57,7 +60,8 @@ struct Tables {
     uint64_t share_ready;
     int4 job[kMaxStages];
     float red[2][kNCW][2];
-    unsigned epoch;
+    float redp[kMaxP1][kNCW];
+    unsigned gen[2];
     int share_n;
     int count, total;
     int wsum[kNCW];
@@ -65,6 +69,7 @@ struct Tables {
     unsigned wpre[kMaxRange / 32 + 1];
     float lg[kMaxRange];
     float pb[kMaxRange];
+    float ba[kMaxRange];
     float hs[kMaxRank];
     int pref[kMaxG];
     int j[kMaxShare];
@@ -73,13 +78,6 @@ struct Tables {
     int state[kMaxShare];
 };
 constexpr size_t kHdr = (sizeof(Tables) + 1023) & ~(size_t)1023;
-
-__device__ __forceinline__ unsigned long long tagged(unsigned epoch, unsigned v)
-{
-    return ((unsigned long long)(((epoch & 0x7fffffffu) << 1) | 1u) << 32) | v;
-}
-
-__device__ __forceinline__ unsigned tag_of(unsigned epoch) { return ((epoch & 0x7fffffffu) << 1) | 1u; }
 
 __device__ __forceinline__ int ld_cg_int(const int *p)
 {
@@ -95,18 +93,33 @@ __device__ __forceinline__ float ld_cg_f32(const float *p)
     return v;
 }
 
-// Bounded wait of one thread for a tagged word of this epoch; returns its value.
-__device__ __forceinline__ unsigned wait_tagged(const unsigned long long *w, unsigned epoch, unsigned *err,
-                                                bool *ok)
+__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
 {
-    const unsigned want = tag_of(epoch);
-    for (long long i = 0; i < kSpinLimit; ++i) {
-        const unsigned long long s = ld_volatile_u64(w);
-        if ((unsigned)(s >> 32) == want) return (unsigned)s;
+    unsigned v;
+    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier, called by one thread per CTA after the CTA's own writes are
+// complete (a CTA barrier before the call).  gen0 is the generation word's
+// value read at kernel start.  Returns false on timeout.
+__device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned gen0, unsigned G, unsigned *err)
+{
+    __threadfence();
+    const unsigned old = atomicAdd(count, 1u);
+    if (old == G - 1u) {
+        *count = 0u;
+        __threadfence();
+        atomicExch(gen, gen0 + 1u);
+        return true;
     }
+    for (long long i = 0; i < kSpinLimit; ++i)
+        if (ld_volatile_u32(gen) != gen0) {
+            __threadfence();
+            return true;
+        }
     atomicOr(err, ERR_TIMEOUT);
-    *ok = false;
-    return 0u;
+    return false;
 }
 
 template <typename PT>
@@ -126,8 +139,9 @@ struct FusedParams {
     int *idx_out;        // ordered active list, or null
     int *n_active;       // or null
     int *cand;           // [F] candidate lists (each CTA writes inside its range)
+    float *cand_bias;    // [F] b_act of each candidate
     float *h;            // [rank]
-    unsigned long long *flag_h, *status;  // [G] each
+    unsigned *status;    // [G] active count of each CTA's range
     WsCtrl *ctrl;
     int d, F, r, act;
     float tau;
@@ -151,9 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
     unsigned *err = &p.ctrl->err;
     const int hk0 = (int)((long long)r * c / G), hk1 = (int)((long long)r * (c + 1) / G);
     const int j0 = (int)((long long)F * c / G), j1 = (int)((long long)F * (c + 1) / G);
-    const int nP1 = hk1 - hk0, nR = j1 - j0;
-    const int nP2 = (nR + kGroup - 1) / kGroup;
+    const int nP1r = hk1 - hk0, nR = j1 - j0;
     const uint32_t p1row = (uint32_t)d * sizeof(PT), p2row = (uint32_t)r * sizeof(PT);
+    const int rp1 = max(1, min(kMaxP1, (int)(stage_bytes / p1row)));  // P1 rows per job
+    const int nP1 = (nP1r + rp1 - 1) / rp1;
+    const int nP2 = (nR + kGroup - 1) / kGroup;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
@@ -164,20 +180,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kMaxShare; i += kThreads) T.state[i] = 0;
-    for (int i = threadIdx.x; i < nR; i += kThreads) T.pb[i] = p.p_bias ? p.p_bias[j0 + i] : 0.f;
+    for (int i = threadIdx.x; i < nR; i += kThreads) {  // layer constants: no need to wait
+        T.pb[i] = p.p_bias ? p.p_bias[j0 + i] : 0.f;
+        T.ba[i] = p.b_act ? p.b_act[j0 + i] : 0.f;
+    }
     __syncthreads();
 
     if (warp == kNCW) {
         // ================================ producer =================================
-        int q = 0;
-        bool failed = false;
         if (lane == 0) {
+            int q = 0;
+            bool failed = false;
             auto acquire = [&](int qq) -> bool {
                 const int s = qq % nstages;
                 return qq < nstages || mbar_wait(&T.empty[s], (unsigned)((qq / nstages) - 1) & 1u, err);
             };
-            // predictor jobs: independent of the previous kernel, issued at once
-            for (int i = 0; i < nP1 + nP2 && !failed; ++i) {
+            if (nP1r) prefetch_l2(p.p1 + (size_t)hk0 * p1row, (uint32_t)nP1r * p1row);
+            if (nR) prefetch_l2(p.p2 + (size_t)j0 * p2row, (uint32_t)nR * p2row);
+            for (int i = 0; i < nP1 + nP2; ++i) {
                 if (!acquire(q)) {
                     failed = true;
                     break;
@@ -185,9 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
                 const int s = q % nstages;
                 uint8_t *st = stages + (size_t)s * stage_bytes;
                 if (i < nP1) {
-                    T.job[s] = make_int4(kJobP1, hk0 + i, 0, 0);
-                    mbar_arrive_expect_tx(&T.full[s], p1row);
-                    bulk_g2s(st, p.p1 + (size_t)(hk0 + i) * p1row, p1row, &T.full[s]);
+                    const int k0 = hk0 + i * rp1, k1 = min(k0 + rp1, hk1);
+                    const uint32_t bytes = (uint32_t)(k1 - k0) * p1row;
+                    T.job[s] = make_int4(kJobP1, k0, k1, 0);
+                    mbar_arrive_expect_tx(&T.full[s], bytes);
+                    bulk_g2s(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s]);
                 } else {
                     const int g0 = j0 + (i - nP1) * kGroup, g1 = min(g0 + kGroup, j1);
                     const uint32_t bytes = (uint32_t)(g1 - g0) * p2row;
@@ -200,6 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
             // FFN jobs, once the consumers have found this CTA's share
             if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
             const int sn = failed ? 0 : T.share_n;
+            for (int i = 0; i < sn; ++i) {  // all the share's rows towards L2 at once
+                const int j = T.j[i];
+                if (j < 0 || j >= F) continue;
+                if constexpr (WT == 2) {
+                    prefetch_l2(p.w_act + (size_t)j * (d / 2), (uint32_t)(d / 2));
+                    if constexpr (GATED) prefetch_l2(p.w_up + (size_t)j * (d / 2), (uint32_t)(d / 2));
+                } else {
+                    prefetch_l2(p.w_act + (size_t)j * R, R);
+                    if constexpr (GATED) prefetch_l2(p.w_up + (size_t)j * R, R);
+                }
+            }
             volatile int *state = T.state;
             int up = 0, ds = 0;
             while (!failed) {
@@ -254,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
                 ++q;
                 if (kind == kJobEnd) break;
             }
-            if (failed) {
+            if (failed) {  // never leave bulk copies in flight into this CTA's shared memory
                 for (int s = 0; s < nstages && s < q; ++s) {
                     const int last = s + ((q - 1 - s) / nstages) * nstages;
                     mbar_wait(&T.full[s], (unsigned)(last / nstages) & 1u, err);
@@ -268,9 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
     const int t = threadIdx.x;
     pdl_wait();
     pdl_trigger();
-    if (t == 0) T.epoch = *reinterpret_cast<volatile unsigned *>(&p.ctrl->epoch);
+    if (t == 0) {
+        T.gen[0] = ld_volatile_u32(&p.ctrl->bar_gen[0]);
+        T.gen[1] = ld_volatile_u32(&p.ctrl->bar_gen[1]);
+    }
 
-    // y = b_down + residual, this CTA's share; made visible before the flag below
+    // y = b_down + residual, this CTA's share (ordered before every CTA's
+    // atomics by barrier A)
     {
         const int nvec = d / 4;
         const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
@@ -286,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
             }
             reinterpret_cast<float4 *>(p.y)[v] = o;
         }
-        __threadfence();
     }
 
     float xr[CH][EPC];
@@ -305,8 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
             acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
         }
     }
-    named_bar_sync(1, kNCT);
-    const unsigned epoch = T.epoch;
     bool ok = true;
     int q = 0, ub = 0;
 
@@ -315,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
         if (lane == 0) mbar_arrive(&T.empty[s]);
     };
 
-    // ---- 1. hidden layer: this CTA's P1 rows ----
+    // ---- 1. hidden layer: this CTA's P1 rows, rp1 rows per job ----
     for (int i = 0; i < nP1 && ok; ++i, ++q) {
         const int s = q % nstages;
         if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
@@ -323,39 +357,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
             break;
         }
         const uint8_t *st = stages + (size_t)s * stage_bytes;
-        float part = 0.f;
+        const int4 job = T.job[s];
+        const int nrow = job.z - job.y;
+        float part[kMaxP1];
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-            const int cc = t + kNCT * u;
-            if (cc < nch) {
+        for (int k = 0; k < kMaxP1; ++k) part[k] = 0.f;
 #pragma unroll
-                for (int g = 0; g < PSEG; ++g)
-                    part += dot16<PT>(*reinterpret_cast<const uint4 *>(st + ((size_t)cc * PSEG + g) * 16),
-                                      &xr[u][g * PEPC]);
+        for (int k = 0; k < kMaxP1; ++k) {
+            if (k < nrow) {
+#pragma unroll
+                for (int u = 0; u < CH; ++u) {
+                    const int cc = t + kNCT * u;
+                    if (cc < nch) {
+#pragma unroll
+                        for (int g = 0; g < PSEG; ++g)
+                            part[k] += dot16<PT>(*reinterpret_cast<const uint4 *>(
+                                                     st + (size_t)k * p1row + ((size_t)cc * PSEG + g) * 16),
+                                                 &xr[u][g * PEPC]);
+                    }
+                }
             }
         }
-        part = warp_sum(part);
-        if (lane == 0) T.red[ub & 1][warp][0] = part;
+#pragma unroll
+        for (int k = 0; k < kMaxP1; ++k) {
+            if (k < nrow) {
+                const float v = warp_sum(part[k]);
+                if (lane == 0) T.redp[k][warp] = v;
+            }
+        }
         named_bar_sync(1, kNCT);
-        if (t == 0) {
+        if (t < nrow) {
             float z = 0.f;
 #pragma unroll
-            for (int w = 0; w < kNCW; ++w) z += T.red[ub & 1][w][0];
-            p.h[T.job[s].y] = fmaxf(z, 0.f);
+            for (int w = 0; w < kNCW; ++w) z += T.redp[t][w];
+            p.h[job.y + t] = fmaxf(z, 0.f);
         }
-        ++ub;
         release(s);
+        named_bar_sync(1, kNCT);  // T.redp is reused by the next job
     }
-    if (t == 0) {
-        __threadfence();
-        st_volatile_u64(&p.flag_h[c], tagged(epoch, 1u));
-    }
-    // barrier A: every CTA's h slice (and y initialisation) is out
-    for (int i = t; i < G; i += kNCT) {
-        bool o2 = true;
-        wait_tagged(&p.flag_h[i], epoch, err, &o2);
-        ok = ok && o2;
-    }
+    // grid barrier A: every CTA's h slice and y initialisation are out
+    named_bar_sync(1, kNCT);
+    if (t == 0 && !grid_barrier(&p.ctrl->bar_count[0], &p.ctrl->bar_gen[0], T.gen[0], (unsigned)G, err)) ok = false;
     named_bar_sync(1, kNCT);
     for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
     named_bar_sync(1, kNCT);
@@ -389,32 +431,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
         if (lane == 0) T.words[wd] = bits;
     }
     named_bar_sync(1, kNCT);
-    if (t == 0) {
-        int run = 0;
-        for (int wd = 0; wd < nw; ++wd) {
-            T.wpre[wd] = run;
-            run += __popc(T.words[wd]);
+    if (t < 32) {  // prefix of the range's words (nw <= 17)
+        const unsigned cw = t < nw ? (unsigned)__popc(T.words[t]) : 0u;
+        unsigned inc = cw;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (t >= o) inc += v;
         }
-        T.count = run;
+        if (t < nw) T.wpre[t] = inc - cw;
+        if (t == 31) T.count = (int)inc;
     }
     named_bar_sync(1, kNCT);
-    // candidate list of this range: ascending active neurons, at cand[j0 ...)
+    // candidate list of this range: ascending active neurons and their biases
     for (int wd = warp; wd < nw; wd += kNCW) {
         const unsigned bits = T.words[wd];
-        if ((bits >> lane) & 1u) p.cand[j0 + T.wpre[wd] + __popc(bits & ((1u << lane) - 1u))] = j0 + wd * 32 + lane;
-    }
-    __threadfence();
-    named_bar_sync(1, kNCT);
-    if (t == 0) st_volatile_u64(&p.status[c], tagged(epoch, (unsigned)T.count));
-
-    // barrier B: every range's count -> exclusive prefix and total
-    for (int i = t; i < G; i += kNCT) {
-        bool o2 = true;
-        T.pref[i] = (int)wait_tagged(&p.status[i], epoch, err, &o2);
-        ok = ok && o2;
+        if ((bits >> lane) & 1u) {
+            const int pos = j0 + (int)T.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
+            p.cand[pos] = j0 + wd * 32 + lane;
+            p.cand_bias[pos] = T.ba[wd * 32 + lane];
+        }
     }
     named_bar_sync(1, kNCT);
-    {   // exclusive scan of the G counts by the consumer threads
+    if (t == 0) {
+        p.status[c] = (unsigned)T.count;
+        if (!grid_barrier(&p.ctrl->bar_count[1], &p.ctrl->bar_gen[1], T.gen[1], (unsigned)G, err)) ok = false;
+    }
+    named_bar_sync(1, kNCT);
+    // every range's count -> exclusive prefix and total
+    for (int i = t; i < G; i += kNCT) T.pref[i] = (int)ld_cg_int(reinterpret_cast<const int *>(p.status) + i);
+    named_bar_sync(1, kNCT);
+    {
         const int per = (G + kNCT - 1) / kNCT;
         const int i0 = min(G, t * per), i1 = min(G, i0 + per);
         int mine = 0;
@@ -441,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
         }
         if (t == 0) {
             T.total = total;
-            if (c == 0) atomicExch(&p.ctrl->epoch, epoch + 1u);  // every CTA has read this launch's epoch
             if (c == G - 1 && p.n_active) *p.n_active = total;
         }
     }
@@ -460,10 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
             const int mid = (lo + hi + 1) >> 1;
             if (T.pref[mid] <= k) lo = mid; else hi = mid - 1;
         }
-        const int rs = (int)((long long)F * lo / G);
-        const int jn = ld_cg_int(p.cand + rs + (k - T.pref[lo]));
-        T.j[i] = jn;
-        T.bias[i] = (p.b_act && jn >= 0 && jn < F) ? p.b_act[jn] : 0.f;
+        const int at = (int)((long long)F * lo / G) + (k - T.pref[lo]);
+        T.j[i] = ld_cg_int(p.cand + at);
+        T.bias[i] = ld_cg_f32(p.cand_bias + at);
     }
     named_bar_sync(1, kNCT);
     if (t == 0) {
@@ -539,13 +584,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
     }
 }
 
-#ifndef PI_FUSED_SMEM_KB
-#define PI_FUSED_SMEM_KB 110
-#endif
-// Shared-memory budget of one CTA: small enough that the next layer's CTA can
-// start its predictor prefetch on the same SM while this one finishes.
-constexpr size_t g_smem_budget = (size_t)PI_FUSED_SMEM_KB * 1024;
-
 template <int WT, typename PT, bool GATED, int CH>
 cudaError_t launch_t(const FusedParams &p, int G, int ns, uint32_t stage_bytes, cudaStream_t s)
 {
@@ -570,6 +608,12 @@ cudaError_t launch_ch(const FusedParams &p, int need, int G, int ns, uint32_t sb
     return cudaErrorNotSupported;
 }
 
+int chunks_per_thread(int wtype, int d)
+{
+    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
+    return (d / epc + kNCT - 1) / kNCT;
+}
+
 }  // namespace
 
 bool fused_layer_supported(int wtype, int ptype, int d, int F, int r)
@@ -578,55 +622,49 @@ bool fused_layer_supported(int wtype, int ptype, int d, int F, int r)
     if (G > kMaxG || r > kMaxRank) return false;
     if (!((wtype == 1 && ptype == 1) || (wtype == 2 && ptype == 1) || (wtype == 0 && ptype == 0))) return false;
     if ((F + G - 1) / G > kMaxRange) return false;
-    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
-    const int need = (d / epc + kNCT - 1) / kNCT;
-    return need <= (wtype == 2 ? 2 : 8);
+    return chunks_per_thread(wtype, d) <= (wtype == 2 ? 2 : 8);
 }
 
-cudaError_t launch_layer_b1(int wtype, int ptype, int gated, int act, const void *p1, const void *p2,
-                            const float *p_bias, float tau, int r, const void *w_up, const void *w_gate,
-                            const void *w_down, const float *b_act, const float *b_down, const float *x,
-                            const float *residual, float *y, int *idx_out, int *n_active, int *cand, float *h,
-                            unsigned long long *flags, WsCtrl *ctrl, int d, int F, cudaStream_t s)
+cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
 {
     const int G = sm_count();
     FusedParams p{};
-    p.p1 = static_cast<const uint8_t *>(p1);
-    p.p2 = static_cast<const uint8_t *>(p2);
-    p.p_bias = p_bias;
-    p.w_act = static_cast<const uint8_t *>(gated ? w_gate : w_up);
-    p.w_up = static_cast<const uint8_t *>(gated ? w_up : nullptr);
-    p.w_down = static_cast<const uint8_t *>(w_down);
-    p.b_act = b_act;
-    p.b_down = b_down;
-    p.x = x;
-    p.residual = residual;
-    p.y = y;
-    p.idx_out = idx_out;
-    p.n_active = n_active;
-    p.cand = cand;
-    p.h = h;
-    p.flag_h = flags;
-    p.status = flags + kMaxG;
-    p.ctrl = ctrl;
-    p.d = d;
-    p.F = F;
-    p.r = r;
-    p.act = act;
-    p.tau = tau;
-    const int esz = ptype == 1 ? 2 : 4;
-    const uint32_t R = row_slot_bytes(wtype, d);
-    uint32_t sb = std::max<uint32_t>({(uint32_t)d * esz, (uint32_t)kGroup * r * esz, (gated ? 2u : 1u) * R});
+    p.p1 = static_cast<const uint8_t *>(a.p1);
+    p.p2 = static_cast<const uint8_t *>(a.p2);
+    p.p_bias = a.p_bias;
+    p.w_act = static_cast<const uint8_t *>(a.gated ? a.w_gate : a.w_up);
+    p.w_up = static_cast<const uint8_t *>(a.gated ? a.w_up : nullptr);
+    p.w_down = static_cast<const uint8_t *>(a.w_down);
+    p.b_act = a.b_act;
+    p.b_down = a.b_down;
+    p.x = a.x;
+    p.residual = a.residual;
+    p.y = a.y;
+    p.idx_out = a.idx_out;
+    p.n_active = a.n_active;
+    p.cand = a.cand;
+    p.cand_bias = a.cand_bias;
+    p.h = a.h;
+    p.status = a.status;
+    p.ctrl = a.ctrl;
+    p.d = a.d;
+    p.F = a.F;
+    p.r = a.r;
+    p.act = a.act;
+    p.tau = a.tau;
+    const int esz = a.ptype == 1 ? 2 : 4;
+    const uint32_t R = row_slot_bytes(a.wtype, a.d);
+    uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
     sb = (sb + 127u) & ~127u;
-    int ns = (int)((g_smem_budget - kHdr) / sb);
-    ns = std::min(ns, kMaxStages);
-    if (ns < 2) {
-        ns = 2;  // wide rows: accept a larger footprint rather than fail
-    }
+    const int need = chunks_per_thread(a.wtype, a.d);
+    // Small register footprints leave room for the next layer's CTA on the same
+    // SM (its predictor prefetch then overlaps this one's FFN phase): keep the
+    // ring small there.  Wide layers cannot share an SM anyway: use a deep ring.
+    const size_t budget = (need <= 2 ? 110 : 200) * 1024;
+    int ns = (int)((budget - kHdr) / sb);
+    ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
-    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
-    const int need = (d / epc + kNCT - 1) / kNCT;
-    switch (wtype * 2 + (gated ? 1 : 0)) {
+    switch (a.wtype * 2 + (a.gated ? 1 : 0)) {
     case 0: return launch_ch<0, float, false>(p, need, G, ns, sb, s);
     case 1: return launch_ch<0, float, true>(p, need, G, ns, sb, s);
     case 2: return launch_ch<1, __half, false>(p, need, G, ns, sb, s);

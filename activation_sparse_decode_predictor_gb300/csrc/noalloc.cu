@@ -27,8 +27,8 @@ namespace {
 
 // Largest layer this entry point accepts: d_ff <= 65536, rank <= 2048, one
 // token.  ws_layout() of that shape needs 256 + 16 KiB + 8 KiB + 256 KiB +
-// 256 bytes, rounded up here to 320 KiB.
-constexpr size_t kStaticWsBytes = 320 * 1024;
+// 256 bytes + 256 KiB, rounded up here to 576 KiB.
+constexpr size_t kStaticWsBytes = 576 * 1024;
 constexpr int kStaticMaxDff = 65536;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
