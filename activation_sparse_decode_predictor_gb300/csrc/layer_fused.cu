@@ -16,9 +16,9 @@
 //   P2 jobs      8 rows of P2 each, for this CTA's contiguous neuron range,
 //   FFN jobs     up/gate rows of this CTA's share of the active neurons, and
 //                the down row of each neuron whose activation is non-zero.
-// On entry, before the programmatic-dependent-launch wait, the producer asks
-// L2 for the CTA's whole predictor share (P1 and P2 do not depend on the
-// previous kernel) and fills the ring; later refills then come from L2.  The
+// On entry, before the programmatic-dependent-launch wait, the producer fills
+// the ring with P1 and P2 rows (they do not depend on the previous kernel) and
+// asks L2 for the rest of the CTA's P2 share; later refills come from L2.  The
 // consumers:
 //   1. compute their P1 rows -> h slice -> global; grid barrier A; load h;
 //   2. compute the logits of their neuron range, threshold, ballot, write the
@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
 
     if (warp == kNCW) {
         // ================================ producer =================================
+        // The producer reads nothing the previous kernel writes (weights only),
+        // so it lets the next kernel launch at once; the consumers do so after
+        // their wait.  The next layer's CTA can then start its own predictor
+        // loads on this SM while this CTA is still working.
+        pdl_trigger();
         if (lane == 0) {
             int q = 0;
             bool failed = false;
@@ -195,9 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
                 const int s = qq % nstages;
                 return qq < nstages || mbar_wait(&T.empty[s], (unsigned)((qq / nstages) - 1) & 1u, err);
             };
-            if (nP1r) prefetch_l2(p.p1 + (size_t)hk0 * p1row, (uint32_t)nP1r * p1row);
-            if (nR) prefetch_l2(p.p2 + (size_t)j0 * p2row, (uint32_t)nR * p2row);
             for (int i = 0; i < nP1 + nP2; ++i) {
+                if (i == min(nstages, nP1 + nP2)) {
+                    // the ring is full: ask L2 for the P2 rows still to come, so
+                    // later refills do not wait for HBM (issued after the ring's
+                    // own copies so those are served first)
+                    const int gnext = j0 + max(0, i - nP1) * kGroup;
+                    if (gnext < j1) prefetch_l2(p.p2 + (size_t)gnext * p2row, (uint32_t)(j1 - gnext) * p2row);
+                }
                 if (!acquire(q)) {
                     failed = true;
                     break;
@@ -660,7 +670,10 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     // Small register footprints leave room for the next layer's CTA on the same
     // SM (its predictor prefetch then overlaps this one's FFN phase): keep the
     // ring small there.  Wide layers cannot share an SM anyway: use a deep ring.
-    const size_t budget = (need <= 2 ? 110 : 200) * 1024;
+#ifndef PI_FUSED_SMALL_RING_KB
+#define PI_FUSED_SMALL_RING_KB 110
+#endif
+    const size_t budget = (size_t)(need <= 2 ? PI_FUSED_SMALL_RING_KB : 200) * 1024;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
