@@ -316,25 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
         T.gen[1] = ld_volatile_u32(&p.ctrl->bar_gen[1]);
     }
 
-    // y = b_down + residual, this CTA's share (ordered before every CTA's
-    // atomics by barrier A)
-    {
-        const int nvec = d / 4;
-        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
-        for (int v = v0 + t; v < v1; v += kNCT) {
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (p.b_down) o = reinterpret_cast<const float4 *>(p.b_down)[v];
-            if (p.residual) {
-                const float4 rz = reinterpret_cast<const float4 *>(p.residual)[v];
-                o.x += rz.x;
-                o.y += rz.y;
-                o.z += rz.z;
-                o.w += rz.w;
-            }
-            reinterpret_cast<float4 *>(p.y)[v] = o;
-        }
-    }
-
     float xr[CH][EPC];
     float acc[CH][EPC];
 #pragma unroll
@@ -405,6 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
         release(s);
         named_bar_sync(1, kNCT);  // T.redp is reused by the next job
     }
+    // y = b_down + residual, this CTA's share (ordered before every CTA's
+    // atomics by barrier A; done here, off the path to the first P1 job)
+    {
+        const int nvec = d / 4;
+        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
+        for (int v = v0 + t; v < v1; v += kNCT) {
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p.b_down) o = reinterpret_cast<const float4 *>(p.b_down)[v];
+            if (p.residual) {
+                const float4 rz = reinterpret_cast<const float4 *>(p.residual)[v];
+                o.x += rz.x;
+                o.y += rz.y;
+                o.z += rz.z;
+                o.w += rz.w;
+            }
+            reinterpret_cast<float4 *>(p.y)[v] = o;
+        }
+    }
+
     // grid barrier A: every CTA's h slice and y initialisation are out
     named_bar_sync(1, kNCT);
     if (t == 0 && !grid_barrier(&p.ctrl->bar_count[0], &p.ctrl->bar_gen[0], T.gen[0], (unsigned)G, err)) ok = false;
@@ -600,6 +600,10 @@ cudaError_t launch_t(const FusedParams &p, int G, int ns, uint32_t stage_bytes, 
     auto k = k_layer_b1<WT, PT, GATED, CH>;
     const size_t smem = kHdr + (size_t)ns * stage_bytes;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // all of the unified L1/shared storage as shared memory, so that two CTAs
+    // (this layer's and the next one's) fit on an SM
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, dim3(G), dim3(kThreads), smem, s, p, ns, stage_bytes);
 }
