@@ -145,13 +145,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete (try_wait
-// itself suspends the thread for a while before reporting "not yet").  Returns
-// false (after raising ERR_TIMEOUT) when the bound is hit.
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `ns` nanoseconds pass, instead of spinning on the
+// shared-memory pipe that the computing warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, unsigned parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete: at most
+// 2^16 suspensions of up to 10 us each (well under a second), then it raises
+// ERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *err)
 {
-    for (long long i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < (1 << 16); ++i)
+        if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
     atomicOr(err, ERR_TIMEOUT);
     return false;
 }

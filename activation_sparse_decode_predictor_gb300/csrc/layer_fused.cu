@@ -70,7 +70,7 @@ struct Tables {
     float lg[kMaxRange];
     float pb[kMaxRange];
     float ba[kMaxRange];
-    float hs[kMaxRank];
+    alignas(16) float hs[kMaxRank];
     int pref[kMaxG];
     int j[kMaxShare];
     float bias[kMaxShare];
@@ -431,10 +431,18 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
         const int row = job.y + warp;  // one row per consumer warp
         if (row < job.z) {
             const uint8_t *pr = st + (size_t)warp * p2row;
-            float sum = 0.f;
-            for (int cc = lane; cc < r / PEPC; cc += 32)
-                sum += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
-            sum = warp_sum(sum);
+            const int nc = r / PEPC;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
+            for (int c0 = lane; c0 < nc; c0 += 128) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (c0 + 32 * u < nc) w[u] = *reinterpret_cast<const uint4 *>(pr + (size_t)(c0 + 32 * u) * 16);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (c0 + 32 * u < nc) s4[u] += dot16<PT>(w[u], &T.hs[(c0 + 32 * u) * PEPC]);
+            }
+            const float sum = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
             if (lane == 0) T.lg[row - j0] = sum + T.pb[row - j0];
         }
         release(s);
