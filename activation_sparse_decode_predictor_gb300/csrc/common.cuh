@@ -23,9 +23,9 @@ struct WsCtrl {
     unsigned spare;
     unsigned done;          // scan: CTAs finished in the running launch
     unsigned epoch;         // scan: launch generation, tags the CTA status words
-    unsigned bar_count[2];  // grid barriers of the one-kernel layer step: arrivals ...
-    unsigned bar_gen[2];    // ... and generation words
-    unsigned pad[56];
+    unsigned long long bar_ctr;  // one-kernel layer step: grid-barrier arrivals (never reset)
+    unsigned bar_seq;            // one-kernel layer step: launches completed (moves barrier targets)
+    unsigned pad[57];
 };
 static_assert(sizeof(WsCtrl) == 256, "control block is 256 bytes");
 

@@ -52,6 +52,7 @@ constexpr int kMaxG = 1024;
 constexpr int kMaxRank = 2048;
 constexpr int kGroup = 8;          // P2 rows per job
 constexpr int kMaxP1 = 8;          // P1 rows per job
+constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
 constexpr int kJobP1 = 1, kJobP2 = 2, kJobUp = 3, kJobDown = 4, kJobEnd = 5;
 
 struct Tables {
@@ -60,8 +61,8 @@ struct Tables {
     uint64_t share_ready;
     int4 job[kMaxStages];
     float red[2][kNCW][2];
-    float redp[kMaxP1][kNCW];
-    unsigned gen[2];
+    float redp[kMaxP1R][kNCW];
+    unsigned long long seq;
     int share_n;
     int count, total;
     int wsum[kNCW];
@@ -100,24 +101,20 @@ __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
     return v;
 }
 
-// Grid barrier, called by one thread per CTA after the CTA's own writes are
-// complete (a CTA barrier before the call).  gen0 is the generation word's
-// value read at kernel start.  Returns false on timeout.
-__device__ bool grid_barrier(unsigned *count, unsigned *gen, unsigned gen0, unsigned G, unsigned *err)
+// Grid barrier, called by one thread per CTA after the CTA's own writes (a CTA
+// barrier before the call makes the other threads' writes part of this
+// thread's release).  Arrivals add to a 64-bit counter that is never reset;
+// the barrier is passed when the counter reaches `target` (a multiple of the
+// grid size derived from the launch sequence number).  Returns false on
+// timeout.
+__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long target, unsigned *err)
 {
-    __threadfence();
-    const unsigned old = atomicAdd(count, 1u);
-    if (old == G - 1u) {
-        *count = 0u;
-        __threadfence();
-        atomicExch(gen, gen0 + 1u);
-        return true;
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+    for (long long i = 0; i < kSpinLimit; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if ((long long)(v - target) >= 0) return true;
     }
-    for (long long i = 0; i < kSpinLimit; ++i)
-        if (ld_volatile_u32(gen) != gen0) {
-            __threadfence();
-            return true;
-        }
     atomicOr(err, ERR_TIMEOUT);
     return false;
 }
@@ -318,10 +315,7 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
     const int t = threadIdx.x;
     pdl_wait();
     pdl_trigger();
-    if (t == 0) {
-        T.gen[0] = ld_volatile_u32(&p.ctrl->bar_gen[0]);
-        T.gen[1] = ld_volatile_u32(&p.ctrl->bar_gen[1]);
-    }
+    if (t == 0) T.seq = ld_volatile_u32(&p.ctrl->bar_seq);
 
     float xr[CH][EPC];
     float acc[CH][EPC];
@@ -356,42 +350,30 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
         }
         const uint8_t *st = stages + (size_t)s * stage_bytes;
         const int4 job = T.job[s];
-        const int nrow = job.z - job.y;
-        float part[kMaxP1];
+        for (int k = 0; k < job.z - job.y; ++k) {
+            float part = 0.f;
 #pragma unroll
-        for (int k = 0; k < kMaxP1; ++k) part[k] = 0.f;
+            for (int u = 0; u < CH; ++u) {
+                const int cc = t + kNCT * u;
+                if (cc < nch) {
 #pragma unroll
-        for (int k = 0; k < kMaxP1; ++k) {
-            if (k < nrow) {
-#pragma unroll
-                for (int u = 0; u < CH; ++u) {
-                    const int cc = t + kNCT * u;
-                    if (cc < nch) {
-#pragma unroll
-                        for (int g = 0; g < PSEG; ++g)
-                            part[k] += dot16<PT>(*reinterpret_cast<const uint4 *>(
-                                                     st + (size_t)k * p1row + ((size_t)cc * PSEG + g) * 16),
-                                                 &xr[u][g * PEPC]);
-                    }
+                    for (int g = 0; g < PSEG; ++g)
+                        part += dot16<PT>(*reinterpret_cast<const uint4 *>(st + (size_t)k * p1row +
+                                                                             ((size_t)cc * PSEG + g) * 16),
+                                          &xr[u][g * PEPC]);
                 }
             }
-        }
-#pragma unroll
-        for (int k = 0; k < kMaxP1; ++k) {
-            if (k < nrow) {
-                const float v = warp_sum(part[k]);
-                if (lane == 0) T.redp[k][warp] = v;
-            }
-        }
-        named_bar_sync(1, kNCT);
-        if (t < nrow) {
-            float z = 0.f;
-#pragma unroll
-            for (int w = 0; w < kNCW; ++w) z += T.redp[t][w];
-            p.h[job.y + t] = fmaxf(z, 0.f);
+            part = warp_sum(part);
+            if (lane == 0) T.redp[job.y - hk0 + k][warp] = part;
         }
         release(s);
-        named_bar_sync(1, kNCT);  // T.redp is reused by the next job
+    }
+    named_bar_sync(1, kNCT);
+    if (t < nP1r) {
+        float z = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNCW; ++w) z += T.redp[t][w];
+        p.h[hk0 + t] = fmaxf(z, 0.f);
     }
     // y = b_down + residual, this CTA's share (ordered before every CTA's
     // atomics by barrier A; done here, off the path to the first P1 job)
@@ -414,10 +396,20 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
 
     // grid barrier A: every CTA's h slice and y initialisation are out
     named_bar_sync(1, kNCT);
-    if (t == 0 && !grid_barrier(&p.ctrl->bar_count[0], &p.ctrl->bar_gen[0], T.gen[0], (unsigned)G, err)) ok = false;
+    const unsigned long long base = (2ull * T.seq) * (unsigned long long)G;
+    if (t == 0 && !grid_barrier(&p.ctrl->bar_ctr, base + (unsigned long long)G, err)) ok = false;
     named_bar_sync(1, kNCT);
     for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
     named_bar_sync(1, kNCT);
+    // this lane's slices of h for the P2 rows, kept in registers (the first
+    // kHreg chunks per lane; wider ranks read the rest from shared memory)
+    constexpr int kHreg = 4;
+    float hreg[kHreg][PEPC];
+    const int nc2 = r / PEPC;
+#pragma unroll
+    for (int u = 0; u < kHreg; ++u)
+#pragma unroll
+        for (int e = 0; e < PEPC; ++e) hreg[u][e] = (lane + 32 * u < nc2) ? T.hs[(lane + 32 * u) * PEPC + e] : 0.f;
 
     // ---- 2. logits of this CTA's neuron range ----
     for (int i = 0; i < nP2 && ok; ++i, ++q) {
@@ -431,17 +423,13 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
         const int row = job.y + warp;  // one row per consumer warp
         if (row < job.z) {
             const uint8_t *pr = st + (size_t)warp * p2row;
-            const int nc = r / PEPC;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
-            for (int c0 = lane; c0 < nc; c0 += 128) {
-                uint4 w[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (c0 + 32 * u < nc) w[u] = *reinterpret_cast<const uint4 *>(pr + (size_t)(c0 + 32 * u) * 16);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (c0 + 32 * u < nc) s4[u] += dot16<PT>(w[u], &T.hs[(c0 + 32 * u) * PEPC]);
-            }
+            for (int u = 0; u < kHreg; ++u)
+                if (lane + 32 * u < nc2)
+                    s4[u] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)(lane + 32 * u) * 16), hreg[u]);
+            for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32)
+                s4[cc & 3] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
             const float sum = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
             if (lane == 0) T.lg[row - j0] = sum + T.pb[row - j0];
         }
@@ -480,7 +468,9 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
     named_bar_sync(1, kNCT);
     if (t == 0) {
         p.status[c] = (unsigned)T.count;
-        if (!grid_barrier(&p.ctrl->bar_count[1], &p.ctrl->bar_gen[1], T.gen[1], (unsigned)G, err)) ok = false;
+        if (!grid_barrier(&p.ctrl->bar_ctr, base + 2ull * (unsigned long long)G, err)) ok = false;
+        // every CTA has read this launch's sequence number: move it on
+        if (c == 0) atomicAdd(&p.ctrl->bar_seq, 1u);
     }
     named_bar_sync(1, kNCT);
     // every range's count -> exclusive prefix and total
@@ -648,7 +638,7 @@ int chunks_per_thread(int wtype, int d)
 bool fused_layer_supported(int wtype, int ptype, int d, int F, int r)
 {
     const int G = sm_count();
-    if (G > kMaxG || r > kMaxRank) return false;
+    if (G > kMaxG || r > kMaxRank || (r + G - 1) / G > kMaxP1R) return false;
     if (!((wtype == 1 && ptype == 1) || (wtype == 2 && ptype == 1) || (wtype == 0 && ptype == 0))) return false;
     if ((F + G - 1) / G > kMaxRange) return false;
     return chunks_per_thread(wtype, d) <= (wtype == 2 ? 2 : 8);
