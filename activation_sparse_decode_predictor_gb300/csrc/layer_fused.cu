@@ -341,46 +341,32 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
         if (lane == 0) mbar_arrive(&T.empty[s]);
     };
 
-    // ---- 1. hidden layer: this CTA's P1 rows (rp1 per job), groups of jobs,
-    //         four rows at a time per thread (independent chains) ----
-    const int grp = max(1, min(4, nstages - 1));
-    for (int i = 0; i < nP1 && ok; i += grp) {
-        const int gn = min(grp, nP1 - i);
-        for (int g = 0; g < gn; ++g)
-            if (!mbar_wait(&T.full[(q + g) % nstages], (unsigned)((q + g) / nstages) & 1u, err)) ok = false;
-        if (!ok) break;
-        const int r0 = i * rp1, r1 = min(nP1r, (i + gn) * rp1);  // CTA-local rows of the group
-        for (int k0 = r0; k0 < r1; k0 += 4) {
-            float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const int k = k0 + kk;
-                if (k < r1) {
-                    const uint8_t *rowp = stages + (size_t)((q + (k - r0) / rp1) % nstages) * stage_bytes +
-                                          (size_t)((k - r0) % rp1) * p1row;
-#pragma unroll
-                    for (int u = 0; u < CH; ++u) {
-                        const int cc = t + kNCT * u;
-                        if (cc < nch) {
-#pragma unroll
-                            for (int g = 0; g < PSEG; ++g)
-                                part[kk] += dot16<PT>(
-                                    *reinterpret_cast<const uint4 *>(rowp + ((size_t)cc * PSEG + g) * 16),
-                                    &xr[u][g * PEPC]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if (k0 + kk < r1) {
-                    const float v = warp_sum(part[kk]);
-                    if (lane == 0) T.redp[k0 + kk][warp] = v;
-                }
-            }
+    // ---- 1. hidden layer: this CTA's P1 rows, rp1 rows per job ----
+    for (int i = 0; i < nP1 && ok; ++i, ++q) {
+        const int s = q % nstages;
+        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
+            ok = false;
+            break;
         }
-        for (int g = 0; g < gn; ++g) release((q + g) % nstages);
-        q += gn;
+        const uint8_t *st = stages + (size_t)s * stage_bytes;
+        const int4 job = T.job[s];
+        for (int k = 0; k < job.z - job.y; ++k) {
+            float part = 0.f;
+#pragma unroll
+            for (int u = 0; u < CH; ++u) {
+                const int cc = t + kNCT * u;
+                if (cc < nch) {
+#pragma unroll
+                    for (int g = 0; g < PSEG; ++g)
+                        part += dot16<PT>(*reinterpret_cast<const uint4 *>(st + (size_t)k * p1row +
+                                                                             ((size_t)cc * PSEG + g) * 16),
+                                          &xr[u][g * PEPC]);
+                }
+            }
+            part = warp_sum(part);
+            if (lane == 0) T.redp[job.y - hk0 + k][warp] = part;
+        }
+        release(s);
     }
     named_bar_sync(1, kNCT);
     if (t < nP1r) {
@@ -425,64 +411,29 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
 #pragma unroll
         for (int e = 0; e < PEPC; ++e) hreg[u][e] = (lane + 32 * u < nc2) ? T.hs[(lane + 32 * u) * PEPC + e] : 0.f;
 
-    // ---- 2. logits of this CTA's neuron range, up to kGrp P2 jobs at a time ----
-    // (each warp takes one row of every job of the group: independent chains)
-    constexpr int kGrp = 4;
-    for (int i = 0; i < nP2 && ok; i += grp) {
-        const int gn = min(grp, nP2 - i);
-        const uint8_t *pr[kGrp];
-        int row[kGrp];
-#pragma unroll
-        for (int g = 0; g < kGrp; ++g) {
-            row[g] = -1;
-            pr[g] = nullptr;
-            if (g < gn) {
-                const int s = (q + g) % nstages;
-                if (!mbar_wait(&T.full[s], (unsigned)((q + g) / nstages) & 1u, err)) {
-                    ok = false;
-                    break;
-                }
-                const int4 job = T.job[s];
-                if (job.y + warp < job.z) {
-                    row[g] = job.y + warp;
-                    pr[g] = stages + (size_t)s * stage_bytes + (size_t)warp * p2row;
-                }
-            }
+    // ---- 2. logits of this CTA's neuron range ----
+    for (int i = 0; i < nP2 && ok; ++i, ++q) {
+        const int s = q % nstages;
+        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
+            ok = false;
+            break;
         }
-        if (!ok) break;
-        float acc2[kGrp][4];
+        const uint8_t *st = stages + (size_t)s * stage_bytes;
+        const int4 job = T.job[s];
+        const int row = job.y + warp;  // one row per consumer warp
+        if (row < job.z) {
+            const uint8_t *pr = st + (size_t)warp * p2row;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
-        for (int g = 0; g < kGrp; ++g)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) acc2[g][u] = 0.f;
-#pragma unroll
-        for (int u = 0; u < kHreg; ++u) {
-            if (lane + 32 * u < nc2) {
-#pragma unroll
-                for (int g = 0; g < kGrp; ++g)
-                    if (row[g] >= 0)
-                        acc2[g][u] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr[g] + (size_t)(lane + 32 * u) * 16),
-                                                hreg[u]);
-            }
+            for (int u = 0; u < kHreg; ++u)
+                if (lane + 32 * u < nc2)
+                    s4[u] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)(lane + 32 * u) * 16), hreg[u]);
+            for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32)
+                s4[cc & 3] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
+            const float sum = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
+            if (lane == 0) T.lg[row - j0] = sum + T.pb[row - j0];
         }
-        for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {
-#pragma unroll
-            for (int g = 0; g < kGrp; ++g)
-                if (row[g] >= 0)
-                    acc2[g][cc & 3] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr[g] + (size_t)cc * 16),
-                                                 &T.hs[cc * PEPC]);
-        }
-#pragma unroll
-        for (int g = 0; g < kGrp; ++g) {
-            if (g < gn) {
-                const float sum = warp_sum((acc2[g][0] + acc2[g][1]) + (acc2[g][2] + acc2[g][3]));
-                if (lane == 0 && row[g] >= 0) T.lg[row[g] - j0] = sum + T.pb[row[g] - j0];
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < kGrp; ++g)
-            if (g < gn) release((q + g) % nstages);
-        q += gn;
+        release(s);
     }
     named_bar_sync(1, kNCT);
     const int nw = (nR + 31) >> 5;
