@@ -53,6 +53,7 @@ constexpr int kMaxRank = 2048;
 constexpr int kGroup = 8;          // P2 rows per job
 constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
+constexpr int kUpRing = 32;        // FFN up rows in flight (> ring stages)
 constexpr int kJobP1 = 1, kJobP2 = 2, kJobUp = 3, kJobDown = 4, kJobEnd = 5;
 
 struct Tables {
@@ -60,8 +61,9 @@ struct Tables {
     uint64_t empty[kMaxStages];
     uint64_t share_ready;
     int4 job[kMaxStages];
-    float red[2][kNCW][2];
     float redp[kMaxP1R][kNCW];
+    float redu[kUpRing][kNCW][2];
+    int upcnt[kUpRing];
     unsigned long long seq;
     int share_n;
     int count, total;
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kMaxShare; i += kThreads) T.state[i] = 0;
+    for (int i = threadIdx.x; i < kUpRing; i += kThreads) T.upcnt[i] = 0;
     for (int i = threadIdx.x; i < nR; i += kThreads) {  // layer constants: no need to wait
         T.pb[i] = p.p_bias ? p.p_bias[j0 + i] : 0.f;
         T.ba[i] = p.b_act ? p.b_act[j0 + i] : 0.f;
@@ -269,8 +272,7 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
                     kind = kJobUp;
                 } else if (ds < sn) {
                     long long spins = 0;
-                    while (state[ds] == 0 && ++spins < kSpinLimit) {
-                    }
+                    while (state[ds] == 0 && ++spins < kSpinLimit) __nanosleep(64);
                     if (state[ds] == 0) {
                         atomicOr(err, ERR_TIMEOUT);
                         failed = true;
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
         }
     }
     bool ok = true;
-    int q = 0, ub = 0;
+    int q = 0;
 
     auto release = [&](int s) {
         __syncwarp();
@@ -411,29 +413,57 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
 #pragma unroll
         for (int e = 0; e < PEPC; ++e) hreg[u][e] = (lane + 32 * u < nc2) ? T.hs[(lane + 32 * u) * PEPC + e] : 0.f;
 
-    // ---- 2. logits of this CTA's neuron range ----
-    for (int i = 0; i < nP2 && ok; ++i, ++q) {
-        const int s = q % nstages;
-        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
-            ok = false;
-            break;
-        }
-        const uint8_t *st = stages + (size_t)s * stage_bytes;
-        const int4 job = T.job[s];
-        const int row = job.y + warp;  // one row per consumer warp
-        if (row < job.z) {
-            const uint8_t *pr = st + (size_t)warp * p2row;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
+    // ---- 2. logits of this CTA's neuron range: each warp takes whole P2 jobs
+    //         (up to 8 rows) round-robin, keeps all rows in flight, and reduces
+    //         the rows together with one transposed butterfly (9 shuffles) ----
+    {
+        static_assert(kGroup == 8, "butterfly below reduces 8 rows");
+        const int q0 = q;
+        for (int i = warp; i < nP2 && ok; i += kNCW) {
+            const int qq = q0 + i;
+            const int s = qq % nstages;
+            if (!mbar_wait(&T.full[s], (unsigned)(qq / nstages) & 1u, err)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *st = stages + (size_t)s * stage_bytes;
+            const int4 job = T.job[s];
+            const int nrow = job.z - job.y;
+            float v[kGroup];
 #pragma unroll
-            for (int u = 0; u < kHreg; ++u)
-                if (lane + 32 * u < nc2)
-                    s4[u] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)(lane + 32 * u) * 16), hreg[u]);
-            for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32)
-                s4[cc & 3] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
-            const float sum = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
-            if (lane == 0) T.lg[row - j0] = sum + T.pb[row - j0];
+            for (int rr = 0; rr < kGroup; ++rr) {
+                v[rr] = 0.f;
+                if (rr < nrow) {
+                    const uint8_t *pr = st + (size_t)rr * p2row;
+#pragma unroll
+                    for (int u = 0; u < kHreg; ++u)
+                        if (lane + 32 * u < nc2)
+                            v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)(lane + 32 * u) * 16),
+                                               hreg[u]);
+                    for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32)
+                        v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
+                }
+            }
+            // lanes exchange halves of their row set: after the three steps
+            // lane l holds row 4*b4 + 2*b3 + b2 (bits of l) summed over the 8
+            // lanes sharing those bits; two more steps finish the sum
+#pragma unroll
+            for (int m = 16, n = kGroup / 2; m >= 4; m >>= 1, n >>= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int k = 0; k < n; ++k) {
+                    const float send = upper ? v[k] : v[k + n];
+                    const float keep = upper ? v[k + n] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+            if ((lane & 3) == 0 && rr < nrow) T.lg[job.y + rr - j0] = v[0] + T.pb[job.y + rr - j0];
+            release(s);
         }
-        release(s);
+        q = q0 + nP2;
     }
     named_bar_sync(1, kNCT);
     const int nw = (nR + 31) >> 5;
@@ -556,24 +586,27 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
             pa = warp_sum(pa);
             if constexpr (GATED) pu = warp_sum(pu);
             if (lane == 0) {
-                T.red[ub & 1][warp][0] = pa;
-                T.red[ub & 1][warp][1] = pu;
-            }
-            named_bar_sync(1, kNCT);
-            if (t == 0) {
-                float z = 0.f, uu = 0.f;
-#pragma unroll
-                for (int w = 0; w < kNCW; ++w) {
-                    z += T.red[ub & 1][w][0];
-                    uu += T.red[ub & 1][w][1];
-                }
-                float a = activate(p.act, z + T.bias[job.y]);
-                if constexpr (GATED) a *= uu;
-                T.a[job.y] = a;
+                // the last warp to contribute finishes the row: no CTA barrier
+                const int e = job.y & (kUpRing - 1);
+                T.redu[e][warp][0] = pa;
+                T.redu[e][warp][1] = pu;
                 __threadfence_block();
-                *reinterpret_cast<volatile int *>(&T.state[job.y]) = (a != 0.f) ? 2 : 1;
+                if (atomicAdd(&T.upcnt[e], 1) == kNCW - 1) {
+                    __threadfence_block();
+                    float z = 0.f, uu = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kNCW; ++w) {
+                        z += T.redu[e][w][0];
+                        uu += T.redu[e][w][1];
+                    }
+                    T.upcnt[e] = 0;
+                    float a = activate(p.act, z + T.bias[job.y]);
+                    if constexpr (GATED) a *= uu;
+                    T.a[job.y] = a;
+                    __threadfence_block();
+                    *reinterpret_cast<volatile int *>(&T.state[job.y]) = (a != 0.f) ? 2 : 1;
+                }
             }
-            ++ub;
         } else {
             const float a = T.a[job.y];
 #pragma unroll
