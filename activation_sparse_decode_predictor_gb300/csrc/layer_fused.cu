@@ -461,7 +461,10 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
             const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
             if ((lane & 3) == 0 && rr < nrow) T.lg[job.y + rr - j0] = v[0] + T.pb[job.y + rr - j0];
-            release(s);
+            // the stage's empty barrier counts one arrival per consumer warp:
+            // this warp consumed it alone, so it arrives for all of them
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cnt(&T.empty[s], kNCW);
         }
         q = q0 + nP2;
     }
