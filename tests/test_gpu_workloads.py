@@ -57,4 +57,5 @@ def test_workload_layer_parity(name):
         n3 = torch.zeros(1, dtype=torch.int32, device="cuda")
         B.pi_predict(lay, x, idx3, n3, ws=ws)
         assert B.pi_sync_status(ws) == 0
-        assert np.array_equal(idx3.cpu().numpy()[: int(n3.item())], got_list)
+        got3 = set(idx3.cpu().numpy()[: int(n3.item())].tolist())
+        assert all(amb[j] for j in got3 ^ ref)      # each path may resolve borderline logits its own way
