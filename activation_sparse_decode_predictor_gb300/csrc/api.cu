@@ -19,8 +19,10 @@ WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
     size_t o = 0;
     L.ctrl = o;
     o += sizeof(WsCtrl);
-    L.status = o;  // scan status words (the one-kernel layer step uses the first #SMs words)
-    o = align256(o + (size_t)std::max((d_ff + 31) / 32, 1024) * 8);
+    L.status = o;  // epoch-tagged status words of the scan kernels
+    o = align256(o + (size_t)((d_ff + 31) / 32) * 8);
+    L.fcount = o;  // plain per-CTA counts of the one-kernel layer step (its own region)
+    o = align256(o + (size_t)1024 * 4);
     L.h = o;
     o = align256(o + (size_t)batch * (size_t)rank * 4);
     L.idx = o;
@@ -284,7 +286,7 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
         a.cand = at<int32_t>(ws, L.idx);
         a.cand_bias = at<float>(ws, L.candb);
         a.h = at<float>(ws, L.h);
-        a.status = at<unsigned>(ws, L.status);
+        a.status = at<unsigned>(ws, L.fcount);
         a.ctrl = at<WsCtrl>(ws, L.ctrl);
         a.d = desc->d_model;
         a.F = desc->d_ff;

@@ -18,6 +18,7 @@ struct WsLayout {
     size_t idx;       // internal active list [d_ff] int32
     size_t nact;      // internal active count (int32)
     size_t candb;     // one-kernel layer step: candidate biases [d_ff] fp32
+    size_t fcount;    // one-kernel layer step: per-CTA active counts [1024] u32
     size_t act;       // union path: activations [d_ff][8] fp32
     size_t total;
 };

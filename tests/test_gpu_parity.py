@@ -315,3 +315,25 @@ def test_ffn_layer_degenerate_ranges(shape):
         idx_res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))),
                            dtype=np.int32)
         assert_ffn_close(y.cpu().numpy(), oracle.sparse_ffn(olay, X[t], idx_res), what=f"{shape} t={t}")
+
+
+def test_layer_and_predict_share_a_workspace():
+    """pi_ffn_layer (one kernel) and pi_predict (separate kernels) called in
+    turn on one workspace: neither may read the other's leftovers."""
+    d, F, r = 512, 6000, 64
+    lay, olay, H = _layer(d, F, r, True, "f16", seed=71)
+    X = synth.tokens(4, d, 72).numpy()
+    ws = B.workspace(B.pi_workspace_bytes(lay, 1))
+    for t in range(4):
+        h, logit_ref, M = oracle.predict(olay, X[t])
+        amb = ambiguous(logit_ref, logit_scale(H, h), olay.threshold)
+        ref = set(np.flatnonzero(M).tolist())
+        x = _cuda(X[t])
+        y = torch.empty(d, dtype=torch.float32, device="cuda")
+        B.pi_ffn_layer(lay, x, y, ws=ws)
+        idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.pi_predict(lay, x, idx, n, ws=ws)
+        assert B.pi_sync_status(ws) == 0
+        got = set(idx.cpu().numpy()[: int(n.item())].tolist())
+        assert all(amb[j] for j in got ^ ref)
