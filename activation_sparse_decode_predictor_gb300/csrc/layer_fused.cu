@@ -418,13 +418,21 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
     //         the rows together with one transposed butterfly (9 shuffles) ----
     {
         static_assert(kGroup == 8, "butterfly below reduces 8 rows");
+        // Rounds of m <= #stages jobs, one per warp, with a consumer barrier
+        // between rounds: a stage's previous job is then always released
+        // before anyone waits on its next one, so a parity wait never looks
+        // two phases ahead (it could not tell them apart).
         const int q0 = q;
-        for (int i = warp; i < nP2 && ok; i += kNCW) {
+        const int mr = min(kNCW, nstages);
+        for (int i0 = 0; i0 < nP2; i0 += mr) {  // uniform trip count: every warp meets every barrier
+            if (i0 > 0) named_bar_sync(1, kNCT);
+            const int i = i0 + warp;
+            if (!ok || warp >= mr || i >= nP2) continue;
             const int qq = q0 + i;
             const int s = qq % nstages;
             if (!mbar_wait(&T.full[s], (unsigned)(qq / nstages) & 1u, err)) {
                 ok = false;
-                break;
+                continue;
             }
             const uint8_t *st = stages + (size_t)s * stage_bytes;
             const int4 job = T.job[s];
