@@ -239,15 +239,20 @@ __global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1
             // FFN jobs, once the consumers have found this CTA's share
             if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
             const int sn = failed ? 0 : T.share_n;
+#ifndef PI_FUSED_PREFETCH_DOWN
+#define PI_FUSED_PREFETCH_DOWN 0
+#endif
             for (int i = 0; i < sn; ++i) {  // all the share's rows towards L2 at once
                 const int j = T.j[i];
                 if (j < 0 || j >= F) continue;
                 if constexpr (WT == 2) {
                     prefetch_l2(p.w_act + (size_t)j * (d / 2), (uint32_t)(d / 2));
                     if constexpr (GATED) prefetch_l2(p.w_up + (size_t)j * (d / 2), (uint32_t)(d / 2));
+                    if (PI_FUSED_PREFETCH_DOWN) prefetch_l2(p.w_down + (size_t)j * (d / 2), (uint32_t)(d / 2));
                 } else {
                     prefetch_l2(p.w_act + (size_t)j * R, R);
                     if constexpr (GATED) prefetch_l2(p.w_up + (size_t)j * R, R);
+                    if (PI_FUSED_PREFETCH_DOWN) prefetch_l2(p.w_down + (size_t)j * R, R);
                 }
             }
             volatile int *state = T.state;
