@@ -729,7 +729,7 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     // predictor loads then overlap this one's FFN phase): keep the ring small
     // there.  Wide layers cannot share an SM anyway: use a deep ring.
 #ifndef PI_FUSED_SMALL_RING_KB
-#define PI_FUSED_SMALL_RING_KB 110
+#define PI_FUSED_SMALL_RING_KB 200
 #endif
     const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
     const size_t budget = (size_t)(two_per_sm(epc, need) ? PI_FUSED_SMALL_RING_KB : 200) * 1024;
