@@ -167,13 +167,41 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, unsigned pari
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete: at most
-// 2^16 suspensions of up to 10 us each (well under a second), then it raises
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+#ifndef PI_MBAR_WAIT_MODE
+#define PI_MBAR_WAIT_MODE 0
+#endif
+#ifndef PI_MBAR_SUSPEND_NS
+#define PI_MBAR_SUSPEND_NS 10000u
+#endif
+
+// Bounded wait for the phase with the given parity to complete (a bounded
+// number of polls, well under a second in total), then it raises
 // ERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *err)
 {
+#if PI_MBAR_WAIT_MODE == 0
     for (int i = 0; i < (1 << 16); ++i)
-        if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
+        if (mbar_try_wait_sleep(bar, parity, PI_MBAR_SUSPEND_NS)) return true;
+#elif PI_MBAR_WAIT_MODE == 1
+    for (long long i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+#else
+    for (long long i = 0; i < kSpinLimit; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        __nanosleep(32);
+    }
+#endif
     atomicOr(err, ERR_TIMEOUT);
     return false;
 }
