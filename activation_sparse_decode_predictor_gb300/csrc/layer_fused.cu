@@ -146,15 +146,10 @@ struct FusedParams {
     float tau;
 };
 
-// Narrow layers (at most 16 columns of x per consumer thread) are compiled for
-// two resident CTAs per SM: the register cap keeps two CTAs' 18 warps within
-// each SM sub-partition's register file, so the next layer's CTA can run its
-// prologue next to this one.
-__host__ __device__ constexpr bool two_per_sm(int epc, int ch) { return epc * ch <= 16; }
-
+// One CTA per SM with a deep ring: measured faster than sharing the SM with
+// the next layer's CTA (which needs a register cap and a shallow ring).
 template <int WT, typename PT, bool GATED, int CH>
-__global__ void __launch_bounds__(kThreads, two_per_sm(Fmt<WT>::EPC, CH) ? 2 : 1)
-    k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
+__global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
 {
     constexpr int EPC = Fmt<WT>::EPC;                // weight elements per 16-byte chunk
     constexpr int PSEG = EPC * (int)sizeof(PT) / 16; // P1 chunks covering one weight chunk's columns
@@ -725,14 +720,7 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
     sb = (sb + 127u) & ~127u;
     const int need = chunks_per_thread(a.wtype, a.d);
-    // Narrow layers leave room for the next layer's CTA on the same SM (its
-    // predictor loads then overlap this one's FFN phase): keep the ring small
-    // there.  Wide layers cannot share an SM anyway: use a deep ring.
-#ifndef PI_FUSED_SMALL_RING_KB
-#define PI_FUSED_SMALL_RING_KB 200
-#endif
-    const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
-    const size_t budget = (size_t)(two_per_sm(epc, need) ? PI_FUSED_SMALL_RING_KB : 200) * 1024;
+    const size_t budget = (size_t)200 * 1024;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
