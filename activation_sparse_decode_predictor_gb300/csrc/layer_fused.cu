@@ -437,20 +437,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nst
             const uint8_t *st = stages + (size_t)s * stage_bytes;
             const int4 job = T.job[s];
             const int nrow = job.z - job.y;
+            // All 8 rows, branch-free, so their loads and FMA chains
+            // interleave: rows past nrow read stage bytes that are in bounds
+            // and are discarded; chunks past the row end load zeros.
             float v[kGroup];
 #pragma unroll
-            for (int rr = 0; rr < kGroup; ++rr) {
-                v[rr] = 0.f;
-                if (rr < nrow) {
-                    const uint8_t *pr = st + (size_t)rr * p2row;
+            for (int rr = 0; rr < kGroup; ++rr) v[rr] = 0.f;
 #pragma unroll
-                    for (int u = 0; u < kHreg; ++u)
-                        if (lane + 32 * u < nc2)
-                            v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)(lane + 32 * u) * 16),
-                                               hreg[u]);
-                    for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32)
-                        v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(pr + (size_t)cc * 16), &T.hs[cc * PEPC]);
+            for (int u = 0; u < kHreg; ++u) {
+                const bool in = lane + 32 * u < nc2;
+#pragma unroll
+                for (int rr = 0; rr < kGroup; ++rr) {
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (in) w = *reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)(lane + 32 * u) * 16);
+                    v[rr] += dot16<PT>(w, hreg[u]);
                 }
+            }
+            for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {  // ranks above 32*kHreg*PEPC
+#pragma unroll
+                for (int rr = 0; rr < kGroup; ++rr)
+                    v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)cc * 16),
+                                       &T.hs[cc * PEPC]);
             }
             // lanes exchange halves of their row set: after the three steps
             // lane l holds row 4*b4 + 2*b3 + b2 (bits of l) summed over the 8
