@@ -146,10 +146,19 @@ struct FusedParams {
     float tau;
 };
 
-// One CTA per SM with a deep ring: measured faster than sharing the SM with
-// the next layer's CTA (which needs a register cap and a shallow ring).
+// Default: one CTA per SM with a deep ring.  With PI_FUSED_COLOCATE, narrow
+// layers (at most 16 columns of x per consumer thread) are instead compiled for
+// two resident CTAs per SM (a register cap that keeps two CTAs' 18 warps within
+// each SM sub-partition's register file) with a shallow ring, so the next
+// layer's CTA starts its predictor loads while this one works.
+#ifndef PI_FUSED_COLOCATE
+#define PI_FUSED_COLOCATE 0
+#endif
+__host__ __device__ constexpr bool colocate(int epc, int ch) { return PI_FUSED_COLOCATE && epc * ch <= 16; }
+
 template <int WT, typename PT, bool GATED, int CH>
-__global__ void __launch_bounds__(kThreads, 1) k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
+__global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
+    k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
 {
     constexpr int EPC = Fmt<WT>::EPC;                // weight elements per 16-byte chunk
     constexpr int PSEG = EPC * (int)sizeof(PT) / 16; // P1 chunks covering one weight chunk's columns
@@ -727,7 +736,8 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
     sb = (sb + 127u) & ~127u;
     const int need = chunks_per_thread(a.wtype, a.d);
-    const size_t budget = (size_t)200 * 1024;
+    const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
+    const size_t budget = (size_t)(colocate(epc, need) ? 110 : 200) * 1024;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
