@@ -328,6 +328,25 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     pdl_trigger();
     if (t == 0) T.seq = ld_volatile_u32(&p.ctrl->bar_seq);
 
+    // this thread's float4 of y = b_down + residual (at most one per thread:
+    // d/4/G <= 16384/4/#SMs < 256), loads issued now, stored after phase 1
+    int yv = -1;
+    float4 yval = make_float4(0.f, 0.f, 0.f, 0.f);
+    {
+        const int nvec = d / 4;
+        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
+        if (v0 + t < v1) {
+            yv = v0 + t;
+            if (p.b_down) yval = reinterpret_cast<const float4 *>(p.b_down)[yv];
+            if (p.residual) {
+                const float4 rz = reinterpret_cast<const float4 *>(p.residual)[yv];
+                yval.x += rz.x;
+                yval.y += rz.y;
+                yval.z += rz.z;
+                yval.w += rz.w;
+            }
+        }
+    }
     float xr[CH][EPC];
     float acc[CH][EPC];
 #pragma unroll
@@ -386,25 +405,9 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         for (int w = 0; w < kNCW; ++w) z += T.redp[t][w];
         p.h[hk0 + t] = fmaxf(z, 0.f);
     }
-    // y = b_down + residual, this CTA's share (ordered before every CTA's
-    // atomics by barrier A; done here, off the path to the first P1 job)
-    {
-        const int nvec = d / 4;
-        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
-        for (int v = v0 + t; v < v1; v += kNCT) {
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (p.b_down) o = reinterpret_cast<const float4 *>(p.b_down)[v];
-            if (p.residual) {
-                const float4 rz = reinterpret_cast<const float4 *>(p.residual)[v];
-                o.x += rz.x;
-                o.y += rz.y;
-                o.z += rz.z;
-                o.w += rz.w;
-            }
-            reinterpret_cast<float4 *>(p.y)[v] = o;
-        }
-    }
-
+    // y = b_down + residual for this CTA's share (loaded right after the
+    // wait, stored here; ordered before every CTA's atomics by barrier A)
+    if (yv >= 0) reinterpret_cast<float4 *>(p.y)[yv] = yval;
     // grid barrier A: every CTA's h slice and y initialisation are out
     named_bar_sync(1, kNCT);
     const unsigned long long base = (2ull * T.seq) * (unsigned long long)G;
@@ -699,6 +702,7 @@ bool fused_layer_supported(int wtype, int ptype, int d, int F, int r)
 {
     const int G = sm_count();
     if (G > kMaxG || r > kMaxRank || (r + G - 1) / G > kMaxP1R) return false;
+    if ((d / 4 + G - 1) / G > kNCT) return false;  // y initialisation: one float4 per consumer thread
     if (!((wtype == 1 && ptype == 1) || (wtype == 2 && ptype == 1) || (wtype == 0 && ptype == 0))) return false;
     if ((F + G - 1) / G > kMaxRange) return false;
     return chunks_per_thread(wtype, d) <= (wtype == 2 ? 2 : 8);
