@@ -31,10 +31,21 @@ WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
     o = align256(o + 16);
     L.candb = o;
     if (batch == 1) o = align256(o + (size_t)d_ff * 4);
-    L.act = o;
-    if (batch > 1) o = align256(o + (size_t)d_ff * 8 * 4);
+    L.act = L.xf = L.uctl = L.zbuf = L.ucnt = o;
+    if (batch > 1) {
+        const size_t tiles = ((size_t)d_ff + 15) / 16;
+        L.act = o;
+        o = align256(o + tiles * 512);
+        L.xf = o;
+        o = align256(o + (((size_t)d_model + 31) / 32) * 1024);
+        L.uctl = o;
+        o = align256(o + 64);
+        L.zbuf = o;
+        o = align256(o + tiles * 1024);
+        L.ucnt = o;
+        o = align256(o + tiles * 4);
+    }
     L.total = o;
-    (void)d_model;
     return L;
 }
 
@@ -163,7 +174,14 @@ pi_status enqueue_sparse(const pi_ffn_desc *D, const float *x, int32_t B, const 
     p.n_active = n_active;
     p.y = y;
     p.ctrl = at<WsCtrl>(ws, L.ctrl);
-    p.act_ws = B > 1 ? at<float>(ws, L.act) : nullptr;
+    if (B > 1) {
+        p.act_ws = at<float>(ws, L.act);
+        p.xf = at<uint32_t>(ws, L.xf);
+        p.uexp = at<int>(ws, L.uctl);
+        p.amax = at<unsigned>(ws, L.uctl + 32);
+        p.zbuf = at<float>(ws, L.zbuf);
+        p.ucnt = at<unsigned>(ws, L.ucnt);
+    }
     p.d = D->d_model;
     p.F = D->d_ff;
     p.act = D->act;

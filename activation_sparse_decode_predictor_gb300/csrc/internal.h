@@ -19,7 +19,11 @@ struct WsLayout {
     size_t nact;      // internal active count (int32)
     size_t candb;     // one-kernel layer step: candidate biases [d_ff] fp32
     size_t fcount;    // one-kernel layer step: per-CTA active counts [1024] u32
-    size_t act;       // union path: activations [d_ff][8] fp32
+    size_t act;       // union path: activations, [ceil(d_ff/16)][4][8][4] fp32 (mma B-operand order)
+    size_t xf;        // union path: x as fp16 hi/lo mma fragments, [ceil(d_model/32)][2][32][4] u32
+    size_t uctl;      // union path: per-token exponents int[8], then max |a| bits u32[8]
+    size_t zbuf;      // union path: per-tile partial sums [ceil(d_ff/16)][2][16][8] fp32 (kept zero)
+    size_t ucnt;      // union path: per-tile arrival counts [ceil(d_ff/16)] u32 (kept zero)
     size_t total;
 };
 
@@ -83,7 +87,12 @@ struct SparseParams {
     const int *n_active;
     float *y;               // [B][d], already holding b_down + residual
     WsCtrl *ctrl;
-    float *act_ws;          // union path scratch [F][8]
+    float *act_ws;          // union path: activations in fragment order
+    uint32_t *xf;           // union path: x fragments
+    int *uexp;              // union path: per-token exponents of x [8]
+    unsigned *amax;         // union path: per-token max |a| (float bits) [8]
+    float *zbuf;            // union path: per-tile partial sums
+    unsigned *ucnt;         // union path: per-tile arrival counts
     int d, F, act, B;
 };
 
