@@ -19,21 +19,33 @@
 // 32-wide block; Q4_0 down-projection weights are dequantised to fp16 in
 // registers (scale * (q - 8), one rounding, relative error <= 2^-11).
 //
+// Data movement.  Rows are gathered by a producer warp with 1-D bulk (TMA)
+// copies, one per row piece, into a shared-memory ring.  A bulk copy costs a
+// roughly fixed issue time (about 45 ns per copy per SM measured on GB300), so
+// pieces are kept at 2-4 KB: smaller pieces cap the stream well below HBM
+// bandwidth whatever the format.
+//
 // Kernels (one stream, chained with programmatic dependent launch):
 //   k_union_prep  x -> fp16 hi/lo fragments in mma B-operand order, exponents.
 //   k_union_up    persistent, one CTA per SM.  Work unit = 16 union rows x one
-//                 chunk of d_model of one matrix; units are ordered chunk-major
-//                 and dealt out to CTAs in contiguous ranges (balanced to one
-//                 unit).  A producer warp streams the 16 rows of each unit into a
-//                 shared-memory ring with 1-D bulk copies; consumer warp w takes
-//                 units w, w+8, ...  Partial sums of a tile are added into a
-//                 per-tile buffer; the warp that completes a tile applies the
-//                 activation and writes a in the down kernel's fragment order.
-//   k_union_down  persistent.  Work unit = 16 union rows x one column block of
-//                 W_down; CTAs take contiguous ranges, each consumer warp owns a
-//                 fixed column slice of the block and accumulates in registers,
-//                 then adds its slice into y with vector atomics when the column
-//                 block changes.
+//                 chunk of d_model (2048 fp16 / 4096 Q4_0 weights) of one
+//                 matrix; units are ordered chunk-major and dealt out to CTAs in
+//                 contiguous ranges.  The 8 consumer warps split each unit's
+//                 chunk and leave their partial sums in one of 4 shared-memory
+//                 slots (mbarrier-tracked); a dedicated reducing warp sums the
+//                 slots and adds them into per-tile buffers, batching up to 4
+//                 units per memory fence, so no consumer ever waits on global
+//                 atomics; the unit that completes a tile has the reducing warp
+//                 apply the activation and write a in the down kernel's
+//                 fragment order.
+//   k_union_down  persistent.  Work unit = 16 union rows x a 2048-column block
+//                 of W_down (+ the tile's activations); CTAs take contiguous
+//                 ranges, each consumer warp owns 256 columns of the block and
+//                 accumulates in registers, then adds its slice into y with
+//                 vector atomics when the column block changes.
+// With more than 4 tokens the hi and lo operand terms go through two mma into
+// the same accumulator (the n8 columns are the 8 tokens); with up to 4 tokens
+// they are separate columns of one mma.
 #include <cuda_fp16.h>
 
 #include "ffn_rows.cuh"
@@ -45,27 +57,35 @@ namespace pi {
 namespace {
 
 constexpr int kUW = 8;                   // consumer warps
-constexpr int kUThreads = kUW * 32 + 32; // + producer warp
+constexpr int kUThreads = kUW * 32 + 32; // + producer warp (down kernel)
+constexpr int kUpThreads = kUThreads + 32; // + reducing warp (up kernel)
 constexpr int kUMaxStages = 32;
 constexpr size_t kHdrU = 2048;           // mbarriers + the producer's neuron-id table
 static_assert(2 * kUMaxStages * 8 + 2 * 128 * 4 <= kHdrU, "header region too small");
 constexpr size_t kSmemBudget = 225 * 1024;
 constexpr int kScaleExp = 10;            // scaled operands have their maximum in [2^10, 2^11)
 constexpr int kBatchJobs = 8;            // producer reads idx for 8 jobs (128 rows) at a time
+constexpr int kSlots = 4;                // up kernel: partial-sum slots in flight
 
-// Up-projection chunks (elements of d_model per unit) and shared-memory rows.
-constexpr int kKsF16 = 512;
-constexpr int kKsQ4 = 1024;
-constexpr int kRsF16Up = kKsF16 * 2 + 64;  // 1088: 16-byte row reads of 8 lanes hit distinct banks
-constexpr int kRsQ4 = 528;                 // 512 code bytes + 16: 32-bit row reads conflict-free
-constexpr int kSsQ4 = 80;                  // 64 scale bytes + 16
+// Up-projection chunks (weights of d_model per unit) and shared-memory row strides.
+constexpr int kKsF16 = 2048;
+constexpr int kKsQ4 = 4096;
+constexpr int kRsF16Up = kKsF16 * 2 + 64;  // 4160: 16-byte row reads of 8 lanes hit distinct banks
+constexpr int kRsQ4Up = kKsQ4 / 2 + 16;    // 2064: 32-bit row reads conflict-free
+constexpr int kSsQ4Up = kKsQ4 / 16 + 16;   // 272: scale rows on distinct banks
 // Down-projection column blocks.
-constexpr int kCwF16 = 512;
-constexpr int kCwQ4 = 1024;
-constexpr int kRsF16Dn = kCwF16 * 2 + 16;  // 1040: ldmatrix rows hit distinct banks
+constexpr int kCw = 2048;                  // columns per block (4 KB fp16 row pieces)
+constexpr int kWc = kCw / kUW;             // 256 columns per consumer warp
+constexpr int kIt = kWc / 16;              // 16 sixteen-column tiles per warp
+constexpr int kRsF16Dn = kCw * 2 + 16;     // 4112: ldmatrix rows hit distinct banks
+constexpr int kRsQ4Dn = kCw / 2 + 16;      // 1040: 32-bit reads of rows 2t.. conflict-free
+constexpr int kSsQ4Dn = kCw / 16 + 16;     // 144
+constexpr int kFlushCols = 64;             // columns per pass of the down kernel's flush
+constexpr uint32_t kTileAct = 512;         // activations of one 16-row tile: [8 tokens][4][4] fp32
 
-constexpr uint32_t up_stage_bytes(bool q4) { return q4 ? 16u * (kRsQ4 + kSsQ4) : 16u * kRsF16Up; }
-constexpr uint32_t dn_stage_bytes(bool q4) { return q4 ? 16u * (kRsQ4 + kSsQ4) : 16u * kRsF16Dn; }
+constexpr uint32_t up_stage_bytes(bool q4) { return q4 ? 16u * (kRsQ4Up + kSsQ4Up) : 16u * kRsF16Up; }
+constexpr uint32_t dn_act_off(bool q4) { return q4 ? 16u * (kRsQ4Dn + kSsQ4Dn) : 16u * kRsF16Dn; }
+constexpr uint32_t dn_stage_bytes(bool q4) { return dn_act_off(q4) + kTileAct; }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
@@ -92,6 +112,8 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
                  : "l"(p));
     return v;
 }
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi)
 {
@@ -138,19 +160,27 @@ __device__ __forceinline__ int frag_k(bool q4, int s, int t, int r, int h)
 // x -> xf[step][group][lane][4] (fp16x2).  Group layout: B <= 4: one group, column
 // g < 4 is hi of token g, column g >= 4 lo of token g - 4.  B > 4: group 0 hi,
 // group 1 lo, column g = token g.  Columns of absent tokens are zero.
+constexpr int kPrepSplit = 16;  // CTAs per token
+
 __global__ void __launch_bounds__(256) k_union_prep(const float *__restrict__ x, int B, int d, int q4,
                                                      uint32_t *__restrict__ xf, int *__restrict__ uexp,
                                                      unsigned *__restrict__ amax)
 {
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.x;
+    const int b = blockIdx.x, part = blockIdx.y;
     const int NG = B > 4 ? 2 : 1;
     __shared__ float red[8];
     float m = 0.f;
     const bool live = b < B;
-    if (live)
-        for (int i = threadIdx.x; i < d; i += blockDim.x) m = fmaxf(m, fabsf(x[(size_t)b * d + i]));
+    if (live) {
+        const float4 *xb = reinterpret_cast<const float4 *>(x + (size_t)b * d);
+#pragma unroll 8
+        for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+            const float4 v = xb[i];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -158,7 +188,7 @@ __global__ void __launch_bounds__(256) k_union_prep(const float *__restrict__ x,
     m = 0.f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
     const int e = live ? scale_exp(m) : 0;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && part == 0) {
         uexp[b] = e;
         amax[b] = 0u;
     }
@@ -166,7 +196,8 @@ __global__ void __launch_bounds__(256) k_union_prep(const float *__restrict__ x,
     const int ghi = b, glo = NG == 1 ? b + 4 : b;
     const int grp_lo = NG == 1 ? 0 : 1;
     const int steps = (d + 31) / 32;
-    for (int v = threadIdx.x; v < steps * 16; v += blockDim.x) {
+    const int v0 = steps * 16 * part / kPrepSplit, v1 = steps * 16 * (part + 1) / kPrepSplit;
+    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
         const int s = v >> 4, t = (v >> 2) & 3, r = v & 3;
         __half hi[2], lo[2];
 #pragma unroll
@@ -181,14 +212,26 @@ __global__ void __launch_bounds__(256) k_union_prep(const float *__restrict__ x,
 }
 
 // ------------------------------------------------------------------------------------
-// Producer warp shared by the up and down kernels: job j of the CTA's range copies
-// the 16 rows idx[16 * tile(j) + r] (rows past n repeat row n - 1, whose values are
-// finite and are multiplied by zero or discarded) into stage j % nstages.  The
-// neuron ids are read one batch of 8 jobs ahead so that their latency overlaps
-// the copies of the batch before.
-template <typename JobTile, typename JobBytes, typename CopyRow>
-__device__ void produce_rows(const SparseParams &p, int n, int cnt, long long u0, int nstages, uint64_t *full,
-                             uint64_t *empty, int *tab, JobTile job_tile, JobBytes job_bytes, CopyRow copy_row)
+// Producer warp shared by the up and down kernels.  Job j of the CTA's range
+// copies the 16 rows idx[16 * tile(j) + r] (rows past n repeat row n - 1, whose
+// values are finite and are multiplied by zero or discarded) into stage
+// j % nstages: lane r < 16 issues row r's bulk copies after lane 0 has set the
+// stage's expected byte count.  The neuron ids are read one batch of 8 jobs
+// ahead so their latency overlaps the copies of the batch before.  The first
+// `pre` jobs are issued before the programmatic-launch wait (weights and ids
+// only, their bytes announced with expect_tx and no arrival); after the wait,
+// late(j, s) copies late_bytes of data that the previous kernel produced, and
+// the stage's single arrival follows.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+template <typename JobTile, typename JobBytes, typename Issue, typename Late>
+__device__ void produce_rows(const SparseParams &p, int n, int cnt, int nstages, int pre, uint32_t late_bytes,
+                             uint64_t *full, uint64_t *empty, int *tab, JobTile job_tile, JobBytes job_bytes,
+                             Issue issue, Late late)
 {
     constexpr int kNone = -2147483647 - 1;  // no job at this position
     const int lane = threadIdx.x & 31;
@@ -200,7 +243,7 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, long long u0
             const int jj = jb + (v >> 4);
             out[i] = kNone;
             if (jj < cnt) {
-                int row = 16 * job_tile(u0 + jj) + (v & 15);
+                int row = 16 * job_tile(jj) + (v & 15);
                 row = row < n ? row : n - 1;
                 out[i] = __ldcg(p.idx + row);
             }
@@ -219,15 +262,25 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, long long u0
             tab[buf * 128 + lane + 32 * i] = j;
         }
     };
-    int pre[4];
-    fetch(0, pre);
-    store(0, pre);
+    pre = min(pre, cnt);
+    auto release_pre = [&]() {
+        pdl_wait();
+        for (int jj = 0; jj < pre; ++jj) {
+            if (lane == 0) mbar_arrive_expect_tx(&full[jj % nstages], late_bytes);
+            __syncwarp();
+            late(jj, jj % nstages);
+        }
+    };
+    int pref[4];
+    fetch(0, pref);
+    store(0, pref);
     __syncwarp();
     bool failed = false;
     int j = 0;
+    if (pre == 0) release_pre();
     for (int jb = 0; jb < cnt && !failed; jb += kBatchJobs) {
         const int buf = (jb / kBatchJobs) & 1;
-        fetch(jb + kBatchJobs, pre);
+        fetch(jb + kBatchJobs, pref);
         const int je = min(cnt, jb + kBatchJobs);
         for (j = jb; j < je; ++j) {
             const int s = j % nstages;
@@ -240,12 +293,20 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, long long u0
                     break;
                 }
             }
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], 16u * job_bytes(u0 + j));
+            const bool early = j < pre;
+            if (lane == 0) {
+                if (early)
+                    mbar_expect_tx(&full[s], job_bytes(j));
+                else
+                    mbar_arrive_expect_tx(&full[s], job_bytes(j) + late_bytes);
+            }
             __syncwarp();
-            if (lane < 16) copy_row(u0 + j, s, lane, tab[buf * 128 + (j - jb) * 16 + lane], &full[s]);
+            issue(j, s, tab + buf * 128 + (j - jb) * 16);
+            if (!early) late(j, s);
+            if (j == pre - 1) release_pre();
         }
         __syncwarp();
-        store(buf ^ 1, pre);
+        store(buf ^ 1, pref);
         __syncwarp();
     }
     if (failed && lane == 0) {
@@ -259,10 +320,11 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, long long u0
 
 // ------------------------------------------------------------------------------------
 template <int WT, bool GATED, int NG>
-__global__ void __launch_bounds__(kUThreads, 1) k_union_up(SparseParams p, int nstages)
+__global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int nstages)
 {
     constexpr bool Q4 = WT == PI_Q4_0;
-    constexpr int KS = Q4 ? kKsQ4 : kKsF16;   // elements of d_model per unit
+    constexpr int KS = Q4 ? kKsQ4 : kKsF16;   // weights of d_model per unit
+    constexpr int SPW = KS / 32 / kUW;        // 32-wide steps per warp and unit
     constexpr int M = GATED ? 2 : 1;          // matrices per row tile
     constexpr uint32_t SB = up_stage_bytes(Q4);
     extern __shared__ __align__(128) uint8_t smem[];
@@ -270,6 +332,9 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_up(SparseParams p, int n
     uint64_t *empty = full + kUMaxStages;
     int *tab = reinterpret_cast<int *>(empty + kUMaxStages);  // [2][128]
     uint8_t *stages = smem + kHdrU;
+    float *red = reinterpret_cast<float *>(stages + (size_t)nstages * SB);  // [kSlots][8 warps][16 rows][8 tokens]
+    __shared__ __align__(8) uint64_t rdy[kSlots];  // all 256 consumer lanes wrote their partial sums
+    __shared__ __align__(8) uint64_t fre[kSlots];  // the unit's reducing warp has read the slot
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = p.d, F = p.F;
     unsigned *err = &p.ctrl->err;
@@ -277,7 +342,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_up(SparseParams p, int n
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kUW);
+        }
+        for (int b = 0; b < kSlots; ++b) {
+            mbar_init(&rdy[b], kUW * 32);
+            mbar_init(&fre[b], 32);
         }
         fence_mbar_init();
     }
@@ -289,82 +358,171 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_up(SparseParams p, int n
     n = n < 0 ? 0 : (n > F ? F : n);
     const int T = (n + 15) >> 4;
     const int C = (d + KS - 1) / KS;
-    const long long per = (long long)T * M;
-    const long long U = per * C;
+    const int per = T * M;                    // units per chunk
+    const long long U = (long long)per * C;
     const int G = gridDim.x;
-    const long long u0 = U * blockIdx.x / G, u1 = U * (blockIdx.x + 1) / G;
-    const int cnt = (int)(u1 - u0);
+    const int u0 = (int)(U * blockIdx.x / G), u1 = (int)(U * (blockIdx.x + 1) / G);
+    const int cnt = u1 - u0;
     if (cnt <= 0) return;
 
+    if (warp == kUW + 1) {
+        // ---------------------------- reducing warp ----------------------------
+        const int rrow = lane >> 1, rtb = 4 * (lane & 1);  // row and first token of this lane
+        float rsc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rsc[i] = ldexpf(1.f, __ldcg(p.uexp + rtb + i));
+        const int B = p.B;
+        for (int jn = 0; jn < cnt;) {
+            int nb = 0;
+            for (; nb < kSlots && jn + nb < cnt; ++nb) {
+                const int jj = jn + nb;
+                const unsigned par = (unsigned)(jj / kSlots) & 1u;
+                if (nb == 0 ? !mbar_wait(&rdy[jj % kSlots], par, err) : !mbar_test_wait(&rdy[jj % kSlots], par)) break;
+            }
+            if (nb == 0) break;  // gave up (error raised)
+            for (int b = 0; b < nb; ++b) {
+                const int jj = jn + b, u = u0 + jj;
+                const float *rb = red + (size_t)(jj % kSlots) * (kUW * 128);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (NG == 2 || rtb == 0) {
+#pragma unroll
+                    for (int w = 0; w < kUW; ++w) {
+                        const float4 pz = *reinterpret_cast<const float4 *>(rb + w * 128 + rrow * 8 + rtb);
+                        v.x += pz.x;
+                        v.y += pz.y;
+                        v.z += pz.z;
+                        v.w += pz.w;
+                    }
+                }
+                mbar_arrive(&fre[jj % kSlots]);
+                if (NG == 2 || rtb == 0) {
+                    v.x *= rsc[0];
+                    v.y *= rsc[1];
+                    v.z *= rsc[2];
+                    v.w *= rsc[3];
+                    const int tile = (u % per) / M, m = u % M;
+                    atomicAdd(reinterpret_cast<float4 *>(p.zbuf + ((size_t)tile * 2 + m) * 128 + rrow * 8 + rtb), v);
+                }
+            }
+            fence_acq_rel_gpu();
+            __syncwarp();
+            unsigned old = 0;
+            if (lane < nb) old = atomicAdd(p.ucnt + ((u0 + jn + lane) % per) / M, 1u);
+            unsigned last = __ballot_sync(0xffffffffu, lane < nb && old == (unsigned)(C * M - 1));
+            if (last) fence_acq_rel_gpu();
+            while (last) {
+                // ---- this batch completed the tile: activation, fragment-order store, reset ----
+                const int b = __ffs(last) - 1;
+                last &= last - 1;
+                const int tile = ((u0 + jn + b) % per) / M;
+                const int row = rrow, tb = rtb;
+                float *z0p = p.zbuf + ((size_t)tile * 2 + 0) * 128 + row * 8 + tb;
+                float *z1p = p.zbuf + ((size_t)tile * 2 + 1) * 128 + row * 8 + tb;
+                const float4 zg = __ldcg(reinterpret_cast<const float4 *>(z0p));
+                float4 zu = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (GATED) zu = __ldcg(reinterpret_cast<const float4 *>(z1p));
+                __stcg(reinterpret_cast<float4 *>(z0p), make_float4(0.f, 0.f, 0.f, 0.f));
+                if constexpr (GATED) __stcg(reinterpret_cast<float4 *>(z1p), make_float4(0.f, 0.f, 0.f, 0.f));
+                const int k = 16 * tile + row;
+                bool valid = k < n;
+                float bias = 0.f;
+                if (valid) {
+                    // an out-of-range neuron id (flagged by the producer, which copied
+                    // row 0 in its place) contributes nothing
+                    const int jid = __ldcg(p.idx + k);
+                    valid = jid >= 0 && jid < F;
+                    if (valid && p.b_act) bias = p.b_act[jid];
+                }
+                const float zgv[4] = {zg.x, zg.y, zg.z, zg.w};
+                const float zuv[4] = {zu.x, zu.y, zu.z, zu.w};
+                float mx[4];
+                const int tq = (row & 7) >> 1, jx = (row & 1) + 2 * (row >> 3);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a = 0.f;
+                    if (valid && tb + i < B) {
+                        a = activate(p.act, zgv[i] + bias);
+                        if constexpr (GATED) a *= zuv[i];
+                    }
+                    p.act_ws[(((size_t)tile * 8 + tb + i) * 4 + tq) * 4 + jx] = a;
+                    mx[i] = fabsf(a);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int o = 2; o < 32; o <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], o));
+                if (lane < 2)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (mx[i] > 0.f) atomicMax(p.amax + tb + i, __float_as_uint(mx[i]));
+                if (lane == 0) p.ucnt[tile] = 0u;
+            }
+            jn += nb;
+        }
+        return;
+    }
+
     if (warp == kUW) {
-        auto job_tile = [&](long long u) { return (int)((u % per) / M); };
-        auto job_bytes = [&](long long u) {
-            const int len = min(KS, d - (int)(u / per) * KS);
-            return Q4 ? (uint32_t)(len / 2 + len / 16) : (uint32_t)len * 2u;
+        auto job_tile = [&](int jj) { return ((u0 + jj) % per) / M; };
+        auto job_bytes = [&](int jj) {
+            const int len = min(KS, d - ((u0 + jj) / per) * KS);
+            return 16u * (Q4 ? (uint32_t)(len / 2 + len / 16) : (uint32_t)len * 2u);
         };
-        auto copy_row = [&](long long u, int s, int r, int jn, uint64_t *bar) {
-            const int c = (int)(u / per);
-            const int m = (int)(u % M);
+        auto issue = [&](int jj, int s, const int *rows) {
+            if (lane >= 16) return;
+            const int u = u0 + jj;
+            const int c = u / per, m = u % M;
             const int k0 = c * KS, len = min(KS, d - k0);
             const uint8_t *W = (GATED && m == 1) ? p.w_up : p.w_act;
             uint8_t *st = stages + (size_t)s * SB;
+            const size_t jn = (size_t)rows[lane];
             if constexpr (Q4) {
-                bulk_g2s(st + r * kRsQ4, W + (size_t)jn * (d / 2) + k0 / 2, (uint32_t)(len / 2), bar);
-                bulk_g2s(st + 16 * kRsQ4 + r * kSsQ4, W + (size_t)F * (d / 2) + (size_t)jn * (d / 16) + k0 / 16,
-                         (uint32_t)(len / 16), bar);
+                bulk_g2s(st + lane * kRsQ4Up, W + jn * (d / 2) + k0 / 2, (uint32_t)(len / 2), &full[s]);
+                bulk_g2s(st + 16 * kRsQ4Up + lane * kSsQ4Up, W + (size_t)F * (d / 2) + jn * (d / 16) + k0 / 16,
+                         (uint32_t)(len / 16), &full[s]);
             } else {
-                bulk_g2s(st + r * kRsF16Up, W + ((size_t)jn * d + k0) * 2, (uint32_t)len * 2u, bar);
+                bulk_g2s(st + lane * kRsF16Up, W + (jn * d + k0) * 2, (uint32_t)len * 2u, &full[s]);
             }
         };
-        produce_rows(p, n, cnt, u0, nstages, full, empty, tab, job_tile, job_bytes, copy_row);
+        produce_rows(p, n, cnt, nstages, 0, 0u, full, empty, tab, job_tile, job_bytes, issue, [](int, int) {});
         return;
     }
 
     // ---------------------------------- consumer warps ----------------------------------
     const int g = lane >> 2, t = lane & 3;
-    // exponents of the two tokens whose sums this lane adds (tokens 2t, 2t+1)
-    const int tk0 = 2 * t;
-    const float sc0 = tk0 < 8 ? ldexpf(1.f, __ldcg(p.uexp + tk0)) : 0.f;
-    const float sc1 = tk0 + 1 < 8 ? ldexpf(1.f, __ldcg(p.uexp + tk0 + 1)) : 0.f;
-    const int B = p.B;
-
-    for (int jj = warp; jj < cnt; jj += kUW) {
+    for (int jj = 0; jj < cnt; ++jj) {
         const int s = jj % nstages;
-        const long long u = u0 + jj;
-        const int c = (int)(u / per);
-        const int tile = (int)((u % per) / M);
-        const int m = (int)(u % M);
+        const int u = u0 + jj;
+        const int c = u / per;
         if (!mbar_wait(&full[s], (unsigned)(jj / nstages) & 1u, err)) break;
         const uint8_t *st = stages + (size_t)s * SB;
         const int k0 = c * KS, len = min(KS, d - k0);
-        float acc[NG][4];
-#pragma unroll
-        for (int q = 0; q < NG; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};  // two mma chains
+        const int q0 = warp * SPW;
+        const int q1 = min(q0 + SPW, (len + 31) / 32);
         const uint8_t *xfp = reinterpret_cast<const uint8_t *>(p.xf) + ((size_t)(k0 / 32) * NG * 32 + lane) * 16;
         if constexpr (!Q4) {
-            const int nsteps = (len + 31) / 32;
             const uint8_t *ra = st + g * kRsF16Up + 16 * t;
             const uint8_t *rb = ra + 8 * kRsF16Up;
 #pragma unroll 4
-            for (int q = 0; q < nsteps; ++q) {
+            for (int q = q0; q < q1; ++q) {
                 uint4 a0 = *reinterpret_cast<const uint4 *>(ra + q * 64);
                 uint4 a1 = *reinterpret_cast<const uint4 *>(rb + q * 64);
                 if (q * 32 + 8 * t >= len) a0 = a1 = make_uint4(0u, 0u, 0u, 0u);  // ragged end of d_model
 #pragma unroll
-                for (int gr = 0; gr < NG; ++gr) {
+                for (int gr = 0; gr < NG; ++gr) {  // NG == 2: hi then lo terms into the same sums
                     const uint4 bx = ldg_nc_v4(xfp + ((size_t)q * NG + gr) * 512);
-                    mma16816(acc[gr], a0.x, a1.x, a0.y, a1.y, bx.x, bx.y);
-                    mma16816(acc[gr], a0.z, a1.z, a0.w, a1.w, bx.z, bx.w);
+                    mma16816(acc, a0.x, a1.x, a0.y, a1.y, bx.x, bx.y);
+                    mma16816(acc2, a0.z, a1.z, a0.w, a1.w, bx.z, bx.w);
                 }
             }
         } else {
-            const int nsteps = len / 32;
-            const uint8_t *ca = st + g * kRsQ4 + 4 * t;
-            const uint8_t *cb = ca + 8 * kRsQ4;
-            const __half *sa = reinterpret_cast<const __half *>(st + 16 * kRsQ4 + g * kSsQ4);
-            const __half *sb = reinterpret_cast<const __half *>(st + 16 * kRsQ4 + (g + 8) * kSsQ4);
+            const uint8_t *ca = st + g * kRsQ4Up + 4 * t;
+            const uint8_t *cb = ca + 8 * kRsQ4Up;
+            const __half *sa = reinterpret_cast<const __half *>(st + 16 * kRsQ4Up + g * kSsQ4Up);
+            const __half *sb = reinterpret_cast<const __half *>(st + 16 * kRsQ4Up + (g + 8) * kSsQ4Up);
 #pragma unroll 4
-            for (int q = 0; q < nsteps; ++q) {
+            for (int q = q0; q < q1; ++q) {
                 const uint32_t w0 = *reinterpret_cast<const uint32_t *>(ca + q * 16);
                 const uint32_t w1 = *reinterpret_cast<const uint32_t *>(cb + q * 16);
                 const float s0 = __half2float(sa[q]), s1 = __half2float(sb[q]);
@@ -376,94 +534,42 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_up(SparseParams p, int n
                     float tmp[4] = {0.f, 0.f, 0.f, 0.f};
                     mma16816(tmp, p0, r0, p1, r1, bx.x, bx.y);
                     mma16816(tmp, p2, r2, p3, r3, bx.z, bx.w);
-                    acc[gr][0] = fmaf(s0, tmp[0], acc[gr][0]);
-                    acc[gr][1] = fmaf(s0, tmp[1], acc[gr][1]);
-                    acc[gr][2] = fmaf(s1, tmp[2], acc[gr][2]);
-                    acc[gr][3] = fmaf(s1, tmp[3], acc[gr][3]);
+                    float *ac = (gr & 1) ? acc2 : acc;
+                    ac[0] = fmaf(s0, tmp[0], ac[0]);
+                    ac[1] = fmaf(s0, tmp[1], ac[1]);
+                    ac[2] = fmaf(s1, tmp[2], ac[2]);
+                    ac[3] = fmaf(s1, tmp[3], ac[3]);
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
 
-        // hi + lo columns -> this lane's sums for tokens 2t, 2t+1 (lanes t < 2 when NG == 1)
+        // -> this warp's partial sums for tokens 2t, 2t+1 (NG == 1: hi + lo columns, lanes t < 2)
         float z[4];
-        bool has;
-        if constexpr (NG == 1) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) z[i] = acc[0][i] + __shfl_xor_sync(0xffffffffu, acc[0][i], 2);
-            has = t < 2;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) z[i] = acc[0][i] + acc[1][i];
-            has = true;
-        }
-        float *zb = p.zbuf + ((size_t)tile * 2 + m) * 128;
-        if (has) {
-            atomicAdd(reinterpret_cast<float2 *>(zb + g * 8 + tk0), make_float2(z[0] * sc0, z[1] * sc1));
-            atomicAdd(reinterpret_cast<float2 *>(zb + (g + 8) * 8 + tk0), make_float2(z[2] * sc0, z[3] * sc1));
-        }
-        __threadfence();
-        __syncwarp();
-        unsigned old = 0;
-        if (lane == 0) old = atomicAdd(p.ucnt + tile, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != (unsigned)(C * M - 1)) continue;
-
-        // ---- this warp completed the tile: activation, fragment-order store, reset ----
-        __threadfence();
-        const int row = lane >> 1, tb = 4 * (lane & 1);
-        float *z0p = p.zbuf + ((size_t)tile * 2 + 0) * 128 + row * 8 + tb;
-        float *z1p = p.zbuf + ((size_t)tile * 2 + 1) * 128 + row * 8 + tb;
-        const float4 zg = __ldcg(reinterpret_cast<const float4 *>(z0p));
-        float4 zu = make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (GATED) zu = __ldcg(reinterpret_cast<const float4 *>(z1p));
-        __stcg(reinterpret_cast<float4 *>(z0p), make_float4(0.f, 0.f, 0.f, 0.f));
-        if constexpr (GATED) __stcg(reinterpret_cast<float4 *>(z1p), make_float4(0.f, 0.f, 0.f, 0.f));
-        const int k = 16 * tile + row;
-        bool valid = k < n;
-        float bias = 0.f;
-        if (valid) {
-            // an out-of-range neuron id (flagged by the producer, which copied row 0
-            // in its place) contributes nothing
-            const int jn = __ldcg(p.idx + k);
-            valid = jn >= 0 && jn < F;
-            if (valid && p.b_act) bias = p.b_act[jn];
-        }
-        const float zgv[4] = {zg.x, zg.y, zg.z, zg.w};
-        const float zuv[4] = {zu.x, zu.y, zu.z, zu.w};
-        float mx[4];
-        const int tq = (row & 7) >> 1, jx = (row & 1) + 2 * (row >> 3);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float a = 0.f;
-            if (valid && tb + i < B) {
-                a = activate(p.act, zgv[i] + bias);
-                if constexpr (GATED) a *= zuv[i];
-            }
-            p.act_ws[(((size_t)tile * 4 + tq) * 8 + tb + i) * 4 + jx] = a;
-            mx[i] = fabsf(a);
+            z[i] = acc[i] + acc2[i];
+            if constexpr (NG == 1) z[i] += __shfl_xor_sync(0xffffffffu, z[i], 2);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int o = 2; o < 32; o <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], o));
-        if (lane < 2)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (mx[i] > 0.f) atomicMax(p.amax + tb + i, __float_as_uint(mx[i]));
-        if (lane == 0) p.ucnt[tile] = 0u;
+        const int sl = jj % kSlots, use = jj / kSlots;
+        float *rb = red + (size_t)sl * (kUW * 128);
+        if (use > 0 && !mbar_wait(&fre[sl], (unsigned)(use - 1) & 1u, err)) break;
+        if (NG == 2 || t < 2) {
+            *reinterpret_cast<float2 *>(rb + warp * 128 + g * 8 + 2 * t) = make_float2(z[0], z[1]);
+            *reinterpret_cast<float2 *>(rb + warp * 128 + (g + 8) * 8 + 2 * t) = make_float2(z[2], z[3]);
+        }
+        mbar_arrive(&rdy[sl]);
     }
 }
 
-// ------------------------------------------------------------------------------------
 template <int WT, int NG>
 __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int nstages)
 {
     constexpr bool Q4 = WT == PI_Q4_0;
-    constexpr int CW = Q4 ? kCwQ4 : kCwF16;   // columns of a block
-    constexpr int IT = Q4 ? 8 : 4;            // 16-column tiles per warp
-    constexpr int WC = IT * 16;               // columns per warp
+    constexpr int CW = kCw;                   // columns of a block
+    constexpr int IT = kIt;                   // 16-column tiles per warp
+    constexpr int WC = kWc;                   // columns per warp
     constexpr uint32_t SB = dn_stage_bytes(Q4);
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -497,24 +603,33 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
     if (cnt <= 0) return;
 
     if (warp == kUW) {
-        auto job_tile = [&](long long u) { return (int)(u % T); };
-        auto job_bytes = [&](long long u) {
-            const int nc = min(CW, d - (int)(u / T) * CW);
-            return Q4 ? (uint32_t)(nc / 2 + nc / 16) : (uint32_t)nc * 2u;
+        auto job_tile = [&](int jj) { return (int)((u0 + jj) % T); };
+        auto job_bytes = [&](int jj) {
+            const int nc = min(CW, d - (int)((u0 + jj) / T) * CW);
+            return 16u * (Q4 ? (uint32_t)(nc / 2 + nc / 16) : (uint32_t)nc * 2u);
         };
-        auto copy_row = [&](long long u, int s, int r, int jn, uint64_t *bar) {
-            const int cb = (int)(u / T);
-            const int c0 = cb * CW, nc = min(CW, d - c0);
+        auto issue = [&](int jj, int s, const int *rows) {
+            if (lane >= 16) return;
+            const long long u = u0 + jj;
+            const int c0 = (int)(u / T) * CW, nc = min(CW, d - c0);
             uint8_t *st = stages + (size_t)s * SB;
+            const size_t jn = (size_t)rows[lane];
             if constexpr (Q4) {
-                bulk_g2s(st + r * kRsQ4, p.w_down + (size_t)jn * (d / 2) + c0 / 2, (uint32_t)(nc / 2), bar);
-                bulk_g2s(st + 16 * kRsQ4 + r * kSsQ4,
-                         p.w_down + (size_t)F * (d / 2) + (size_t)jn * (d / 16) + c0 / 16, (uint32_t)(nc / 16), bar);
+                bulk_g2s(st + lane * kRsQ4Dn, p.w_down + jn * (d / 2) + c0 / 2, (uint32_t)(nc / 2), &full[s]);
+                bulk_g2s(st + 16 * kRsQ4Dn + lane * kSsQ4Dn, p.w_down + (size_t)F * (d / 2) + jn * (d / 16) + c0 / 16,
+                         (uint32_t)(nc / 16), &full[s]);
             } else {
-                bulk_g2s(st + r * kRsF16Dn, p.w_down + ((size_t)jn * d + c0) * 2, (uint32_t)nc * 2u, bar);
+                bulk_g2s(st + lane * kRsF16Dn, p.w_down + (jn * d + c0) * 2, (uint32_t)nc * 2u, &full[s]);
             }
         };
-        produce_rows(p, n, cnt, u0, nstages, full, empty, tab, job_tile, job_bytes, copy_row);
+        // the tile's activations (written by the up kernel), one 512-byte copy
+        auto late = [&](int jj, int s) {
+            if (lane != 16) return;
+            const int tile = (int)((u0 + jj) % T);
+            bulk_g2s(stages + (size_t)s * SB + dn_act_off(Q4),
+                     reinterpret_cast<const uint8_t *>(p.act_ws) + (size_t)tile * kTileAct, kTileAct, &full[s]);
+        };
+        produce_rows(p, n, cnt, nstages, nstages, kTileAct, full, empty, tab, job_tile, job_bytes, issue, late);
         return;
     }
 
@@ -526,55 +641,54 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
     const float inv = ldexpf(1.f, -scale_exp(__uint_as_float(__ldcg(p.amax + tokB))));
     const float sc0 = ldexpf(1.f, scale_exp(__uint_as_float(__ldcg(p.amax + 2 * t))));
     const float sc1 = ldexpf(1.f, scale_exp(__uint_as_float(__ldcg(p.amax + 2 * t + 1))));
-    float *fb = reinterpret_cast<float *>(stages + (size_t)nstages * SB) + (size_t)warp * 8 * WC;
+    float *fb = reinterpret_cast<float *>(stages + (size_t)nstages * SB) + (size_t)warp * 8 * kFlushCols;
     const int B = p.B;
 
-    float acc[IT][NG][4];
+    float acc[IT][4];
     auto zero_acc = [&]() {
 #pragma unroll
-        for (int i = 0; i < IT; ++i)
-#pragma unroll
-            for (int q = 0; q < NG; ++q) acc[i][q][0] = acc[i][q][1] = acc[i][q][2] = acc[i][q][3] = 0.f;
+        for (int i = 0; i < IT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     };
     // Adds this warp's slice of column block cb into y (through shared memory, so
     // that the atomics are 16-byte vectors).
     auto flush = [&](int cb) {
         const int c0 = cb * CW + warp * WC;
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
-            float v[4];
-            if constexpr (NG == 1) {
+        for (int ps = 0; ps < WC / kFlushCols; ++ps) {
+            // pass ps: the tiles whose columns fall in [64 ps, 64 ps + 64) of the warp slice
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = acc[i][0][e] + __shfl_xor_sync(0xffffffffu, acc[i][0][e], 2);
-            } else {
+            for (int i = ps * 4; i < ps * 4 + 4; ++i) {
+                float v[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = acc[i][0][e] + acc[i][1][e];
-            }
-            if (NG == 2 || t < 2) {
-                int col0, col1;  // columns of rows g and g + 8 of tile i within the warp slice
-                if constexpr (Q4) {
-                    const int h = i >> 2, mm = i & 3;
-                    col0 = 64 * h + 32 * (g >> 2) + 4 * (g & 3) + mm;
-                    col1 = col0 + 16;
-                } else {
-                    col0 = 16 * i + g;
-                    col1 = col0 + 8;
+                for (int e = 0; e < 4; ++e) {
+                    v[e] = acc[i][e];
+                    if constexpr (NG == 1) v[e] += __shfl_xor_sync(0xffffffffu, v[e], 2);
                 }
-                fb[(2 * t) * WC + col0] = v[0] * sc0;
-                fb[(2 * t + 1) * WC + col0] = v[1] * sc1;
-                fb[(2 * t) * WC + col1] = v[2] * sc0;
-                fb[(2 * t + 1) * WC + col1] = v[3] * sc1;
+                if (NG == 2 || t < 2) {
+                    int col0, col1;  // columns of rows g and g + 8 of tile i, within the pass
+                    if constexpr (Q4) {
+                        col0 = 32 * (g >> 2) + 4 * (g & 3) + (i & 3);
+                        col1 = col0 + 16;
+                    } else {
+                        col0 = 16 * (i & 3) + g;
+                        col1 = col0 + 8;
+                    }
+                    fb[(2 * t) * kFlushCols + col0] = v[0] * sc0;
+                    fb[(2 * t + 1) * kFlushCols + col0] = v[1] * sc1;
+                    fb[(2 * t) * kFlushCols + col1] = v[2] * sc0;
+                    fb[(2 * t + 1) * kFlushCols + col1] = v[3] * sc1;
+                }
             }
+            __syncwarp();
+            for (int e = lane; e < B * (kFlushCols / 4); e += 32) {
+                const int tok = e / (kFlushCols / 4), c4 = e % (kFlushCols / 4);
+                const int col = c0 + ps * kFlushCols + 4 * c4;
+                if (col < d)
+                    atomicAdd(reinterpret_cast<float4 *>(p.y + (size_t)tok * d + col),
+                              *reinterpret_cast<const float4 *>(fb + tok * kFlushCols + 4 * c4));
+            }
+            __syncwarp();
         }
-        __syncwarp();
-        for (int e = lane; e < B * (WC / 4); e += 32) {
-            const int tok = e / (WC / 4), c4 = e % (WC / 4);
-            const int col = c0 + 4 * c4;
-            if (col < d)
-                atomicAdd(reinterpret_cast<float4 *>(p.y + (size_t)tok * d + col),
-                          *reinterpret_cast<const float4 *>(fb + tok * WC + 4 * c4));
-        }
-        __syncwarp();
     };
 
     zero_acc();
@@ -598,13 +712,13 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
         const bool live = cb * CW + warp * WC < d;
         if (live) {
             // B operand: a[k][tok] for k = 2t, 2t+1, 2t+8, 2t+9 of this tile, split hi/lo
-            const float4 av = __ldcg(reinterpret_cast<const float4 *>(p.act_ws) + ((size_t)tile * 4 + t) * 8 + tokB);
+            const float4 av = *reinterpret_cast<const float4 *>(st + dn_act_off(Q4) + (tokB * 4 + t) * 16);
             __half h0, h1, h2, h3, l0, l1, l2, l3;
             split_f16(av.x * inv, h0, l0);
             split_f16(av.y * inv, h1, l1);
             split_f16(av.z * inv, h2, l2);
             split_f16(av.w * inv, h3, l3);
-            uint32_t bf[NG][2];
+            uint32_t bf[NG][2];  // NG == 2: [0] hi terms, [1] lo terms, both into the same sums
             if constexpr (NG == 1) {
                 const bool lo = g >= 4;
                 bf[0][0] = lo ? pack_h2(l0, l1) : pack_h2(h0, h1);
@@ -626,22 +740,22 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_trans(base + 32u * i, a0, a1, a2, a3);
 #pragma unroll
-                    for (int q = 0; q < NG; ++q) mma16816(acc[i][q], a0, a1, a2, a3, bf[q][0], bf[q][1]);
+                    for (int q = 0; q < NG; ++q) mma16816(acc[i], a0, a1, a2, a3, bf[q][0], bf[q][1]);
                 }
             } else {
-                const uint8_t *codes = st + 64 * warp + 4 * g;
-                const uint8_t *scl = st + 16 * kRsQ4;
+                const uint8_t *codes = st + (WC / 2) * warp + 4 * g;
+                const uint8_t *scl = st + 16 * kRsQ4Dn;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(codes + (2 * t) * kRsQ4 + 32 * h);
-                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(codes + (2 * t + 1) * kRsQ4 + 32 * h);
-                    const uint32_t wc = *reinterpret_cast<const uint32_t *>(codes + (2 * t + 8) * kRsQ4 + 32 * h);
-                    const uint32_t wd = *reinterpret_cast<const uint32_t *>(codes + (2 * t + 9) * kRsQ4 + 32 * h);
-                    const int blk = 4 * warp + 2 * h + (g >> 2);
-                    const __half2 sA = __halves2half2(*reinterpret_cast<const __half *>(scl + (2 * t) * kSsQ4 + 2 * blk),
-                                                      *reinterpret_cast<const __half *>(scl + (2 * t + 1) * kSsQ4 + 2 * blk));
-                    const __half2 sB = __halves2half2(*reinterpret_cast<const __half *>(scl + (2 * t + 8) * kSsQ4 + 2 * blk),
-                                                      *reinterpret_cast<const __half *>(scl + (2 * t + 9) * kSsQ4 + 2 * blk));
+                for (int h = 0; h < WC / 64; ++h) {
+                    const uint32_t wa = *reinterpret_cast<const uint32_t *>(codes + (2 * t) * kRsQ4Dn + 32 * h);
+                    const uint32_t wb = *reinterpret_cast<const uint32_t *>(codes + (2 * t + 1) * kRsQ4Dn + 32 * h);
+                    const uint32_t wc = *reinterpret_cast<const uint32_t *>(codes + (2 * t + 8) * kRsQ4Dn + 32 * h);
+                    const uint32_t wd = *reinterpret_cast<const uint32_t *>(codes + (2 * t + 9) * kRsQ4Dn + 32 * h);
+                    const int blk = (WC / 32) * warp + 2 * h + (g >> 2);
+                    const __half2 sA = __halves2half2(*reinterpret_cast<const __half *>(scl + (2 * t) * kSsQ4Dn + 2 * blk),
+                                                      *reinterpret_cast<const __half *>(scl + (2 * t + 1) * kSsQ4Dn + 2 * blk));
+                    const __half2 sB = __halves2half2(*reinterpret_cast<const __half *>(scl + (2 * t + 8) * kSsQ4Dn + 2 * blk),
+                                                      *reinterpret_cast<const __half *>(scl + (2 * t + 9) * kSsQ4Dn + 2 * blk));
                     const uint32_t x01 = __byte_perm(wa, wb, 0x5410), y01 = __byte_perm(wa, wb, 0x7632);
                     const uint32_t x89 = __byte_perm(wc, wd, 0x5410), y89 = __byte_perm(wc, wd, 0x7632);
 #pragma unroll
@@ -661,7 +775,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
                         a[3] = *reinterpret_cast<const uint32_t *>(&d3);
 #pragma unroll
                         for (int q = 0; q < NG; ++q)
-                            mma16816(acc[4 * h + mm][q], a[0], a[1], a[2], a[3], bf[q][0], bf[q][1]);
+                            mma16816(acc[4 * h + mm], a[0], a[1], a[2], a[3], bf[q][0], bf[q][1]);
                     }
                 }
             }
@@ -682,16 +796,17 @@ template <int WT, bool GATED, int NG>
 cudaError_t launch_up(const SparseParams &p, cudaStream_t s)
 {
     constexpr uint32_t SB = up_stage_bytes(WT == PI_Q4_0);
-    const size_t fit = (kSmemBudget - kHdrU) / SB;
+    constexpr size_t rbytes = (size_t)kSlots * kUW * 128 * 4;  // the partial-sum slots
+    const size_t fit = (kSmemBudget - kHdrU - rbytes) / SB;
     const int ns = (int)(fit < (size_t)kUMaxStages ? fit : (size_t)kUMaxStages);
-    const size_t smem = kHdrU + (size_t)ns * SB;
+    const size_t smem = kHdrU + (size_t)ns * SB + rbytes;
     static bool once = false;
     if (!once) {
         cudaError_t e = set_smem(k_union_up<WT, GATED, NG>, smem);
         if (e != cudaSuccess) return e;
         once = true;
     }
-    return launch_pdl(k_union_up<WT, GATED, NG>, dim3(sm_count()), dim3(kUThreads), smem, s, p, ns);
+    return launch_pdl(k_union_up<WT, GATED, NG>, dim3(sm_count()), dim3(kUpThreads), smem, s, p, ns);
 }
 
 template <int WT, int NG>
@@ -699,7 +814,7 @@ cudaError_t launch_down(const SparseParams &p, cudaStream_t s)
 {
     constexpr bool Q4 = WT == PI_Q4_0;
     constexpr uint32_t SB = dn_stage_bytes(Q4);
-    constexpr size_t fbytes = (size_t)kUW * 8 * (Q4 ? 128 : 64) * 4;
+    constexpr size_t fbytes = (size_t)kUW * 8 * kFlushCols * 4;
     const size_t fit = (kSmemBudget - kHdrU - fbytes) / SB;
     const int ns = (int)(fit < (size_t)kUMaxStages ? fit : (size_t)kUMaxStages);
     const size_t smem = kHdrU + (size_t)ns * SB + fbytes;
@@ -730,7 +845,7 @@ cudaError_t launch_sparse_union(int wtype, int gated, const SparseParams &p, cud
 {
     if (wtype != PI_F16 && wtype != PI_Q4_0) return cudaErrorNotSupported;
     if (p.B < 2 || p.B > 8) return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(k_union_prep, dim3(8), dim3(256), 0, s, p.x, p.B, p.d, wtype == PI_Q4_0 ? 1 : 0,
+    cudaError_t e = launch_pdl(k_union_prep, dim3(8, kPrepSplit), dim3(256), 0, s, p.x, p.B, p.d, wtype == PI_Q4_0 ? 1 : 0,
                                p.xf, p.uexp, p.amax);
     if (e != cudaSuccess) return e;
     return wtype == PI_Q4_0 ? launch_union_wt<PI_Q4_0>(gated, p, s) : launch_union_wt<PI_F16>(gated, p, s);

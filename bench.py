@@ -39,7 +39,12 @@ from activation_sparse_decode_predictor_gb300 import binding as B  # noqa: E402
 from activation_sparse_decode_predictor_gb300 import synth  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["sparse_ffn.cu", "common.cuh", "internal.h"]
+# sources of the kernel each roofline line describes (a committed ncu traffic
+# figure counts only while its recorded hash matches these files)
+KERNEL_SOURCES = {
+    "k_layer_b1": ["layer_fused.cu", "ffn_rows.cuh", "common.cuh", "internal.h"],
+    "k_union": ["union_mma.cu", "ffn_rows.cuh", "common.cuh", "internal.h"],
+}
 
 
 def parse():
@@ -54,6 +59,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="decode tokens per step (default: the workload's)")
     ap.add_argument("--quick", action="store_true", help="main timed step only (for profiling runs)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="tokens decoded together through the union path (default: the workload's)")
     return ap.parse_args()
 
 
@@ -72,24 +79,24 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "activation_sparse_decode_predictor_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
-    """DRAM bytes per launch of the sparse-FFN kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", f"k_sparse_b1_{workload}.md")
+def committed_traffic(kernel, tag):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    profiles/<kernel>_<tag>.md, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{tag}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
-    if m and s and s.group(1) == kernel_source_hash():
+    if m and s and s.group(1) == kernel_source_hash(kernel):
         return float(m.group(1))
     return None
 
@@ -143,21 +150,37 @@ def dist_env():
 
 
 # ------------------------------------------------------------------------------------ workload
-def needed_bytes(w, n_pred, n_down):
-    """Algorithmic bytes of one token through one layer: predictor weights,
-    the predicted rows of the up/gate projections (+4 B of index each), the
-    down rows of neurons whose activation is non-zero, x in and y out."""
+def needed_bytes(w, n_pred, n_down, batch=1):
+    """Algorithmic bytes of one group of `batch` tokens through one layer:
+    predictor weights (read once for the group), the predicted (union) rows of
+    the up/gate projections (+4 B of index each), the down rows of neurons whose
+    activation is non-zero for at least one token, x in and y out."""
     s_p = 4 if w.wtype == "f32" else 2
     R = {"f32": 4 * w.d_model, "f16": 2 * w.d_model, "q4_0": w.d_model // 32 * 18}[w.wtype]
     g = 2 if w.gated else 1
     pred = (w.rank * w.d_model + w.d_ff * w.rank) * s_p
-    ffn = n_pred * (R * g + 4) + n_down * R + w.batch * w.d_model * 4 * 2
+    ffn = n_pred * (R * g + 4) + n_down * R + batch * w.d_model * 4 * 2
     return pred, ffn
+
+
+def q4_dequant_torch(blob, rows, cols):
+    """Q4_0 split blob -> fp32 matrix with plain torch ops (statistics only)."""
+    codes = blob[: rows * cols // 2].view(rows, cols // 32, 16)
+    scales = blob[rows * cols // 2:].view(torch.float16).view(rows, cols // 32, 1).float()
+    q = torch.cat([codes & 15, codes >> 4], dim=2).float() - 8.0
+    return (q * scales).reshape(rows, cols)
 
 
 def setup_ours(w, replicas, dev):
     torch.cuda.set_device(dev)
     L0 = synth.workload_layer(w, 0, device=f"cuda:{dev}")
+    if w.wtype == "q4_0":
+        # the generator returns fp16 matrices; store them as Q4_0 with the library's quantiser
+        for k in ("w_up", "w_gate", "w_down"):
+            if L0[k] is not None:
+                L0[k] = B.pi_quantize_q4_0(L0[k])
+        L0["wtype_code"] = B.PI_Q4_0
+        torch.cuda.synchronize()
     reps = []
     for k in range(replicas):
         Lk = {key: (v.clone() if isinstance(v, torch.Tensor) else v) for key, v in L0.items()}
@@ -166,33 +189,40 @@ def setup_ours(w, replicas, dev):
     return L0, reps, X
 
 
-def active_stats(w, L0, layer, X, ws):
-    """Per token: predicted active count, the count with non-zero activation,
-    recall and precision of the predictor against the true ReLU mask.  Uses
-    the library for the prediction and torch only to count."""
+def active_stats(w, L0, layer, X, ws, ws1, batch):
+    """Per group of `batch` tokens: predicted (union) active count and the count
+    of those rows with a non-zero activation for some token of the group; per
+    token: recall and precision of the predictor against the true ReLU mask.
+    Uses the library for the predictions and torch only to count."""
     T = X.shape[0]
+    G = T // batch
     F = w.d_ff
-    idx = torch.zeros(T, F, dtype=torch.int32, device=X.device)
-    n = torch.zeros(T, dtype=torch.int32, device=X.device)
+    idx = torch.zeros(G, F, dtype=torch.int32, device=X.device)
+    n = torch.zeros(G, dtype=torch.int32, device=X.device)
+    for gi in range(G):
+        xg = X[gi * batch:(gi + 1) * batch] if batch > 1 else X[gi]
+        B.pi_predict(layer, xg, idx[gi], n[gi:gi + 1], ws=ws)
+    idx1 = torch.zeros(F, dtype=torch.int32, device=X.device)
+    n1 = torch.zeros(T, dtype=torch.int32, device=X.device)
+    own = torch.zeros(T, F, dtype=torch.bool, device=X.device)
     for t in range(T):
-        B.pi_predict(layer, X[t], idx[t], n[t:t + 1], ws=ws)
+        B.pi_predict(layer, X[t], idx1, n1[t:t + 1], ws=ws1)
+        own[t, idx1[: int(n1[t])].long()] = True
     torch.cuda.synchronize()
-    w_act = (L0["w_gate"] if w.gated else L0["w_up"]).float()
+    w_act = L0["w_gate"] if w.gated else L0["w_up"]
+    w_act = q4_dequant_torch(w_act, F, w.d_model) if w.wtype == "q4_0" else w_act.float()
     z = X @ w_act.T + L0["b_act"]
     true = z > 0
-    n_pred, n_down, rec, prec = [], [], [], []
-    for t in range(T):
-        nt = int(n[t])
-        sel = idx[t, :nt].long()
-        pm = torch.zeros(F, dtype=torch.bool, device=X.device)
-        pm[sel] = True
+    n_pred, n_down = [], []
+    for gi in range(G):
+        nt = int(n[gi])
+        sel = idx[gi, :nt].long()
         n_pred.append(nt)
-        n_down.append(int(true[t, sel].sum()))
-        inter = int((pm & true[t]).sum())
-        rec.append(inter / max(1, int(true[t].sum())))
-        prec.append(inter / max(1, nt))
-    return idx, n, np.array(n_pred), np.array(n_down), float(np.mean(rec)), float(np.mean(prec)), \
-        float(true.float().mean())
+        n_down.append(int(true[gi * batch:(gi + 1) * batch][:, sel].any(dim=0).sum()))
+    inter = (own & true).sum(dim=1).float()
+    rec = float((inter / true.sum(dim=1).clamp(min=1)).mean())
+    prec = float((inter / own.sum(dim=1).clamp(min=1)).mean())
+    return idx, n, np.array(n_pred), np.array(n_down), rec, prec, float(true.float().mean())
 
 
 def capture(fn, stream):
@@ -245,8 +275,15 @@ def oracle_sample(w, L0_host, X_host, budget_s):
     return (time.perf_counter() - t0) / done * 1e6, done
 
 
-def host_layer(L0):
+def host_layer(L0, w=None):
+    """Host copy of a layer for the oracle; a Q4_0 workload's fp16 matrices are
+    quantised by the oracle's own quantiser."""
     H = {k: (v.detach().cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in L0.items()}
+    if w is not None and w.wtype == "q4_0":
+        import oracle
+        for k in ("w_up", "w_gate", "w_down"):
+            if H[k] is not None and H[k].dtype != np.uint8:
+                H[k] = oracle.q4_0_quantize(H[k].astype(np.float32))
     return H
 
 
@@ -258,7 +295,7 @@ def run_reference(args, w):
     import oracle
     oracle.build()
     L0 = synth.workload_layer(w, 0, device="cpu")
-    H = host_layer(L0)
+    H = host_layer(L0, w)
     X = synth.workload_tokens(w, device="cpu").numpy()
     per_step = []
     tokens_per_sample = None
@@ -297,21 +334,28 @@ def run_ours(args, w):
     L0, reps, X = setup_ours(w, args.replicas, dev)
     if args.tokens:
         X = X[:args.tokens].contiguous()
-    T = X.shape[0]
+    bsz = args.batch or w.batch
+    T = X.shape[0] // bsz * bsz
+    X = X[:T].contiguous()
+    G = T // bsz                                     # groups of bsz tokens decoded together
     d = w.d_model
     stream = torch.cuda.Stream()
-    ws = B.workspace(B.pi_workspace_bytes(reps[0][1], 1), X.device)
+    ws = B.workspace(B.pi_workspace_bytes(reps[0][1], bsz), X.device)
+    ws1 = ws if bsz == 1 else B.workspace(B.pi_workspace_bytes(reps[0][1], 1), X.device)
     Y = torch.zeros(T, d, dtype=torch.float32, device=X.device)
+    Xg = [X[gi * bsz:(gi + 1) * bsz] if bsz > 1 else X[gi] for gi in range(G)]
+    Yg = [Y[gi * bsz:(gi + 1) * bsz] if bsz > 1 else Y[gi] for gi in range(G)]
 
     # statistics of the active sets (outside any timed region)
-    idx_all, n_all, n_pred, n_down, recall, precision, true_density = active_stats(w, L0, reps[0][1], X, ws)
-    pred_b, ffn_b = needed_bytes(w, n_pred, n_down)
-    bytes_tok = pred_b + ffn_b                       # per token, arrays
-    mean_bytes = float(np.mean(bytes_tok))
+    idx_all, n_all, n_pred, n_down, recall, precision, true_density = active_stats(w, L0, reps[0][1], X, ws, ws1,
+                                                                                   bsz)
+    pred_b, ffn_b = needed_bytes(w, n_pred, n_down, bsz)
+    bytes_grp = pred_b + ffn_b                       # per group, arrays
+    mean_bytes = float(np.mean(bytes_grp)) / bsz     # per token
 
     def step():
-        for t in range(T):
-            B.pi_ffn_layer(reps[t % len(reps)][1], X[t], Y[t], ws=ws)
+        for gi in range(G):
+            B.pi_ffn_layer(reps[gi % len(reps)][1], Xg[gi], Yg[gi], ws=ws)
 
     g_step = capture(step, stream)
     with Clocks(dev) as clk:
@@ -335,20 +379,20 @@ def run_ours(args, w):
 
     # the dominant kernel alone: the sparse FFN on the predicted lists (same rotation)
     def sparse_only():
-        for t in range(T):
-            B.pi_sparse_ffn(reps[t % len(reps)][1], X[t], idx_all[t], n_all[t:t + 1], Y[t], ws=ws)
+        for gi in range(G):
+            B.pi_sparse_ffn(reps[gi % len(reps)][1], Xg[gi], idx_all[gi], n_all[gi:gi + 1], Yg[gi], ws=ws)
 
     def predict_only():
-        for t in range(T):
-            B.pi_predict(reps[t % len(reps)][1], X[t], idx_all[t], n_all[t:t + 1], ws=ws)
+        for gi in range(G):
+            B.pi_predict(reps[gi % len(reps)][1], Xg[gi], idx_all[gi], n_all[gi:gi + 1], ws=ws)
 
     ksteps = max(10, args.steps // 4)
     g_sp = capture(sparse_only, stream)
     ms_sp = time_graph(g_sp, ksteps, args.warmup, stream) / ksteps
     g_pr = capture(predict_only, stream)
     ms_pr = time_graph(g_pr, ksteps, args.warmup, stream) / ksteps
-    us_sp = ms_sp * 1000.0 / T
-    us_pr = ms_pr * 1000.0 / T
+    us_sp = ms_sp * 1000.0 / G                      # per group
+    us_pr = ms_pr * 1000.0 / G
     ffn_gbs = float(np.mean(ffn_b)) / (us_sp * 1e-6) / 1e9
     pred_gbs = float(pred_b) / (us_pr * 1e-6) / 1e9
     layer_gbs = mean_bytes / (us_tok * world * 1e-6) / 1e9
@@ -359,10 +403,12 @@ def run_ours(args, w):
     Xd = torch.empty_like(X)
     e2e_steps = max(3, args.steps // 20)
     with torch.cuda.stream(stream):
+        Xdg = [Xd[gi * bsz:(gi + 1) * bsz] if bsz > 1 else Xd[gi] for gi in range(G)]
+
         def e2e_step():
             Xd.copy_(Xh, non_blocking=True)
-            for t in range(T):
-                B.pi_ffn_layer(reps[t % len(reps)][1], Xd[t], Y[t], ws=ws)
+            for gi in range(G):
+                B.pi_ffn_layer(reps[gi % len(reps)][1], Xdg[gi], Yg[gi], ws=ws)
             Yh.copy_(Y, non_blocking=True)
         for _ in range(2):
             e2e_step()
@@ -380,10 +426,23 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         oracle.build()
-        us_cpu, ntok = oracle_sample(w, host_layer(L0), X.cpu().numpy(), args.cpu_seconds)
+        H0 = host_layer(L0) if w.wtype != "q4_0" else host_layer(synth.workload_layer(w, 0, device="cpu"), w)
+        us_cpu, ntok = oracle_sample(w, H0, X.cpu().numpy(), args.cpu_seconds)
         cpu = {"value": us_cpu, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
                "sample": f"first {ntok} of {T} tokens through one layer (predictor, compaction, sparse FFN), "
                          "single-threaded C oracle, fp64"}
+
+    if bsz == 1:
+        # one kernel per token and layer: the whole step is k_layer_b1 back to back
+        launches_per_group = 1
+        roofline = {"bound": "hbm", "kernel": "k_layer_b1 (pi_ffn_layer)", "achieved": layer_gbs,
+                    "traffic": committed_traffic("k_layer_b1", w.name)}
+    else:
+        # predictor (2 kernels) + k_union_prep + k_union_up + k_union_down per group
+        launches_per_group = 5
+        roofline = {"bound": "hbm", "kernel": "k_union_prep + k_union_up + k_union_down (pi_sparse_ffn)",
+                    "achieved": ffn_gbs, "traffic": committed_traffic("k_union", f"{w.name}_b{bsz}")}
+    roofline.update({"peak": peak, "unit": "GB/s", "frac": roofline["achieved"] / peak, "peak_source": peak_src})
 
     if rank == 0:
         line = {
@@ -392,22 +451,21 @@ def run_ours(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.wtype == "f16" else w.wtype,
             "data": "synthetic",
             "config": {"workload": w.name, "d_model": d, "d_ff": w.d_ff, "rank": w.rank, "gated": w.gated,
-                       "weights": w.wtype, "accumulate": "f32", "batch": w.batch, "tokens_per_step": T,
+                       "weights": w.wtype, "accumulate": "f32", "batch": bsz, "tokens_per_step": T,
                        "sparsity": w.sparsity, "layer_replicas": len(reps),
                        "l2": f"inputs larger than L2: {len(reps)} rotating layer copies, "
                              f"{len(reps) * mean_bytes / 1e6:.0f} MB needed bytes per rotation",
                        "n_active_mean": float(np.mean(n_pred)), "n_nonzero_mean": float(np.mean(n_down)),
                        "true_density": true_density, "predictor_recall": recall, "predictor_precision": precision,
                        "needed_bytes_per_token": mean_bytes, "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "k_sparse_b1 (pi_sparse_ffn)", "achieved": ffn_gbs,
-                         "peak": peak, "unit": "GB/s", "frac": ffn_gbs / peak,
-                         "traffic": committed_traffic(w.name), "peak_source": peak_src},
-            "kernels": {"predict_us": us_pr, "predict_gbs": pred_gbs, "predict_frac": pred_gbs / peak,
+            "roofline": roofline,
+            "kernels": {"per": "token" if bsz == 1 else f"group of {bsz} tokens",
+                        "predict_us": us_pr, "predict_gbs": pred_gbs, "predict_frac": pred_gbs / peak,
                         "sparse_ffn_us": us_sp, "sparse_ffn_gbs": ffn_gbs, "layer_gbs": layer_gbs,
                         "layer_frac": layer_gbs / peak},
             "e2e": {"value": us_e2e, "unit": "us/layer/token", "h2d_bytes_per_step": int(Xh.numel() * 4),
-                    "d2h_bytes_per_step": int(Yh.numel() * 4), "path": "pi_ffn_layer per token, direct calls"},
-            "gpu_launches": 3 * T * args.steps,
+                    "d2h_bytes_per_step": int(Yh.numel() * 4), "path": "pi_ffn_layer per group, direct calls"},
+            "gpu_launches": launches_per_group * G * args.steps,
             "clocks": clk.summary(),
             "device_status": st,
         }
