@@ -380,6 +380,18 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
                 if (nb == 0 ? !mbar_wait(&rdy[jj % kSlots], par, err) : !mbar_test_wait(&rdy[jj % kSlots], par)) break;
             }
             if (nb == 0) break;  // gave up (error raised)
+            // neuron ids and biases of this lane's row in every tile of the batch, issued
+            // now so their latency hides behind the atomics and the fence below
+            int jid[kSlots];
+            float bias[kSlots];
+#pragma unroll
+            for (int b = 0; b < kSlots; ++b) {
+                const int k = 16 * (((u0 + jn + b) % per) / M) + rrow;
+                jid[b] = (b < nb && k < n) ? __ldcg(p.idx + k) : -1;
+            }
+#pragma unroll
+            for (int b = 0; b < kSlots; ++b)
+                bias[b] = (jid[b] >= 0 && jid[b] < F && p.b_act) ? __ldg(p.b_act + jid[b]) : 0.f;
             for (int b = 0; b < nb; ++b) {
                 const int jj = jn + b, u = u0 + jj;
                 const float *rb = red + (size_t)(jj % kSlots) * (kUW * 128);
@@ -408,44 +420,45 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
             __syncwarp();
             unsigned old = 0;
             if (lane < nb) old = atomicAdd(p.ucnt + ((u0 + jn + lane) % per) / M, 1u);
-            unsigned last = __ballot_sync(0xffffffffu, lane < nb && old == (unsigned)(C * M - 1));
-            if (last) fence_acq_rel_gpu();
-            while (last) {
-                // ---- this batch completed the tile: activation, fragment-order store, reset ----
-                const int b = __ffs(last) - 1;
-                last &= last - 1;
-                const int tile = ((u0 + jn + b) % per) / M;
-                const int row = rrow, tb = rtb;
-                float *z0p = p.zbuf + ((size_t)tile * 2 + 0) * 128 + row * 8 + tb;
-                float *z1p = p.zbuf + ((size_t)tile * 2 + 1) * 128 + row * 8 + tb;
-                const float4 zg = __ldcg(reinterpret_cast<const float4 *>(z0p));
-                float4 zu = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (GATED) zu = __ldcg(reinterpret_cast<const float4 *>(z1p));
-                __stcg(reinterpret_cast<float4 *>(z0p), make_float4(0.f, 0.f, 0.f, 0.f));
-                if constexpr (GATED) __stcg(reinterpret_cast<float4 *>(z1p), make_float4(0.f, 0.f, 0.f, 0.f));
-                const int k = 16 * tile + row;
-                bool valid = k < n;
-                float bias = 0.f;
-                if (valid) {
-                    // an out-of-range neuron id (flagged by the producer, which copied
-                    // row 0 in its place) contributes nothing
-                    const int jid = __ldcg(p.idx + k);
-                    valid = jid >= 0 && jid < F;
-                    if (valid && p.b_act) bias = p.b_act[jid];
-                }
-                const float zgv[4] = {zg.x, zg.y, zg.z, zg.w};
-                const float zuv[4] = {zu.x, zu.y, zu.z, zu.w};
-                float mx[4];
-                const int tq = (row & 7) >> 1, jx = (row & 1) + 2 * (row >> 3);
+            const unsigned last = __ballot_sync(0xffffffffu, lane < nb && old == (unsigned)(C * M - 1));
+            if (last) {
+                // ---- tiles completed by this batch: activation, fragment-order store, reset ----
+                fence_acq_rel_gpu();
+                float4 zg[kSlots], zu[kSlots];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float a = 0.f;
-                    if (valid && tb + i < B) {
-                        a = activate(p.act, zgv[i] + bias);
-                        if constexpr (GATED) a *= zuv[i];
+                for (int b = 0; b < kSlots; ++b) {
+                    zg[b] = zu[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if ((last >> b) & 1u) {
+                        const float *zt = p.zbuf + (size_t)(((u0 + jn + b) % per) / M) * 256 + rrow * 8 + rtb;
+                        zg[b] = __ldcg(reinterpret_cast<const float4 *>(zt));
+                        if constexpr (GATED) zu[b] = __ldcg(reinterpret_cast<const float4 *>(zt + 128));
                     }
-                    p.act_ws[(((size_t)tile * 8 + tb + i) * 4 + tq) * 4 + jx] = a;
-                    mx[i] = fabsf(a);
+                }
+                float mx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int b = 0; b < kSlots; ++b) {
+                    if (!((last >> b) & 1u)) continue;
+                    const int tile = ((u0 + jn + b) % per) / M;
+                    float *zt = p.zbuf + (size_t)tile * 256 + rrow * 8 + rtb;
+                    __stcg(reinterpret_cast<float4 *>(zt), make_float4(0.f, 0.f, 0.f, 0.f));
+                    if constexpr (GATED) __stcg(reinterpret_cast<float4 *>(zt + 128), make_float4(0.f, 0.f, 0.f, 0.f));
+                    // an out-of-range neuron id (flagged by the producer, which copied row 0
+                    // in its place) contributes nothing
+                    const bool valid = jid[b] >= 0 && jid[b] < F;
+                    const float zgv[4] = {zg[b].x, zg[b].y, zg[b].z, zg[b].w};
+                    const float zuv[4] = {zu[b].x, zu[b].y, zu[b].z, zu[b].w};
+                    const int tq = (rrow & 7) >> 1, jx = (rrow & 1) + 2 * (rrow >> 3);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float a = 0.f;
+                        if (valid && rtb + i < B) {
+                            a = activate(p.act, zgv[i] + bias[b]);
+                            if constexpr (GATED) a *= zuv[i];
+                        }
+                        p.act_ws[(((size_t)tile * 8 + rtb + i) * 4 + tq) * 4 + jx] = a;
+                        mx[i] = fmaxf(mx[i], fabsf(a));
+                    }
+                    if (lane == b) p.ucnt[tile] = 0u;
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -454,8 +467,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
                 if (lane < 2)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        if (mx[i] > 0.f) atomicMax(p.amax + tb + i, __float_as_uint(mx[i]));
-                if (lane == 0) p.ucnt[tile] = 0u;
+                        if (mx[i] > 0.f) atomicMax(p.amax + rtb + i, __float_as_uint(mx[i]));
             }
             jn += nb;
         }
@@ -490,30 +502,51 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
 
     // ---------------------------------- consumer warps ----------------------------------
     const int g = lane >> 2, t = lane & 3;
+    constexpr bool XREG = !(Q4 && NG == 2);  // x fragments held in registers (not for Q4_0 at 5-8 tokens)
+    uint4 xr[XREG ? SPW : 1][NG];
+    int xc = -1;
     for (int jj = 0; jj < cnt; ++jj) {
         const int s = jj % nstages;
         const int u = u0 + jj;
         const int c = u / per;
+        const int q0 = warp * SPW;
+        if constexpr (XREG) {
+            // this warp's x fragments for chunk c: loaded before the stage wait, and kept
+            // while consecutive units share the chunk (units are ordered chunk-major)
+            if (c != xc) {
+                const int nq = (min(KS, d - c * KS) + 31) / 32;
+                const uint8_t *xfc = reinterpret_cast<const uint8_t *>(p.xf) + ((size_t)(c * KS / 32) * NG * 32 + lane) * 16;
+#pragma unroll
+                for (int i = 0; i < SPW; ++i)
+#pragma unroll
+                    for (int gr = 0; gr < NG; ++gr)
+                        xr[i][gr] = q0 + i < nq ? ldg_nc_v4(xfc + ((size_t)(q0 + i) * NG + gr) * 512)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+                xc = c;
+            }
+        }
         if (!mbar_wait(&full[s], (unsigned)(jj / nstages) & 1u, err)) break;
         const uint8_t *st = stages + (size_t)s * SB;
         const int k0 = c * KS, len = min(KS, d - k0);
         float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};  // two mma chains
-        const int q0 = warp * SPW;
         const int q1 = min(q0 + SPW, (len + 31) / 32);
         const uint8_t *xfp = reinterpret_cast<const uint8_t *>(p.xf) + ((size_t)(k0 / 32) * NG * 32 + lane) * 16;
         if constexpr (!Q4) {
             const uint8_t *ra = st + g * kRsF16Up + 16 * t;
             const uint8_t *rb = ra + 8 * kRsF16Up;
-#pragma unroll 4
-            for (int q = q0; q < q1; ++q) {
-                uint4 a0 = *reinterpret_cast<const uint4 *>(ra + q * 64);
-                uint4 a1 = *reinterpret_cast<const uint4 *>(rb + q * 64);
-                if (q * 32 + 8 * t >= len) a0 = a1 = make_uint4(0u, 0u, 0u, 0u);  // ragged end of d_model
 #pragma unroll
-                for (int gr = 0; gr < NG; ++gr) {  // NG == 2: hi then lo terms into the same sums
-                    const uint4 bx = ldg_nc_v4(xfp + ((size_t)q * NG + gr) * 512);
-                    mma16816(acc, a0.x, a1.x, a0.y, a1.y, bx.x, bx.y);
-                    mma16816(acc2, a0.z, a1.z, a0.w, a1.w, bx.z, bx.w);
+            for (int i = 0; i < SPW; ++i) {
+                const int q = q0 + i;
+                if (q < q1) {
+                    uint4 a0 = *reinterpret_cast<const uint4 *>(ra + q * 64);
+                    uint4 a1 = *reinterpret_cast<const uint4 *>(rb + q * 64);
+                    if (q * 32 + 8 * t >= len) a0 = a1 = make_uint4(0u, 0u, 0u, 0u);  // ragged end of d_model
+#pragma unroll
+                    for (int gr = 0; gr < NG; ++gr) {  // NG == 2: hi then lo terms into the same sums
+                        const uint4 bx = xr[i][gr];
+                        mma16816(acc, a0.x, a1.x, a0.y, a1.y, bx.x, bx.y);
+                        mma16816(acc2, a0.z, a1.z, a0.w, a1.w, bx.z, bx.w);
+                    }
                 }
             }
         } else {
@@ -521,8 +554,10 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
             const uint8_t *cb = ca + 8 * kRsQ4Up;
             const __half *sa = reinterpret_cast<const __half *>(st + 16 * kRsQ4Up + g * kSsQ4Up);
             const __half *sb = reinterpret_cast<const __half *>(st + 16 * kRsQ4Up + (g + 8) * kSsQ4Up);
-#pragma unroll 4
-            for (int q = q0; q < q1; ++q) {
+#pragma unroll
+            for (int i = 0; i < SPW; ++i) {
+                const int q = q0 + i;
+                if (q >= q1) break;
                 const uint32_t w0 = *reinterpret_cast<const uint32_t *>(ca + q * 16);
                 const uint32_t w1 = *reinterpret_cast<const uint32_t *>(cb + q * 16);
                 const float s0 = __half2float(sa[q]), s1 = __half2float(sb[q]);
@@ -530,7 +565,11 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
                 const uint32_t r0 = q4_pair(w1), r1 = q4_pair(w1 >> 4), r2 = q4_pair(w1 >> 8), r3 = q4_pair(w1 >> 12);
 #pragma unroll
                 for (int gr = 0; gr < NG; ++gr) {
-                    const uint4 bx = ldg_nc_v4(xfp + ((size_t)q * NG + gr) * 512);
+                    uint4 bx;
+                    if constexpr (XREG)
+                        bx = xr[i][gr];
+                    else
+                        bx = ldg_nc_v4(xfp + ((size_t)q * NG + gr) * 512);
                     float tmp[4] = {0.f, 0.f, 0.f, 0.f};
                     mma16816(tmp, p0, r0, p1, r1, bx.x, bx.y);
                     mma16816(tmp, p2, r2, p3, r3, bx.z, bx.w);
