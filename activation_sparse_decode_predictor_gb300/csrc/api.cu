@@ -31,19 +31,24 @@ WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
     o = align256(o + 16);
     L.candb = o;
     if (batch == 1) o = align256(o + (size_t)d_ff * 4);
-    L.act = L.xf = L.uctl = L.zbuf = L.ucnt = o;
+    L.act = L.xf = L.uctl = L.zbuf = L.ucnt = L.xfh = L.umask = o;
     if (batch > 1) {
         const size_t tiles = ((size_t)d_ff + 15) / 16;
+        const size_t gemm_tiles = ((size_t)(d_ff > rank ? d_ff : rank) + 15) / 16;  // FFN up or predictor
         L.act = o;
         o = align256(o + tiles * 512);
         L.xf = o;
         o = align256(o + (((size_t)d_model + 31) / 32) * 1024);
         L.uctl = o;
-        o = align256(o + 64);
+        o = align256(o + 96);
         L.zbuf = o;
-        o = align256(o + tiles * 1024);
+        o = align256(o + gemm_tiles * 1024);
         L.ucnt = o;
-        o = align256(o + tiles * 4);
+        o = align256(o + gemm_tiles * 4);
+        L.xfh = o;
+        o = align256(o + (((size_t)(rank > 0 ? rank : 0) + 31) / 32) * 1024);
+        L.umask = o;
+        o = align256(o + (size_t)d_ff);
     }
     L.total = o;
     return L;
@@ -133,6 +138,37 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
                           cudaStream_t s)
 {
     const WsLayout L = ws_layout(D->d_model, D->d_ff, D->rank, B);
+    if (B > 1 && D->ptype == PI_F16) {
+        // several tokens: both predictor contractions on tensor cores, then one scan
+        UnionPredArgs a{};
+        a.p1 = D->p1;
+        a.p2 = D->p2;
+        a.p_bias = D->p_bias;
+        a.tau = D->threshold;
+        a.x = x;
+        a.B = B;
+        a.d = D->d_model;
+        a.r = D->rank;
+        a.F = D->d_ff;
+        a.h = at<float>(ws, L.h);
+        a.logits = logits;
+        a.mask = mask ? mask : at<uint8_t>(ws, L.umask);
+        a.xf_x = at<uint32_t>(ws, L.xf);
+        a.xf_h = at<uint32_t>(ws, L.xfh);
+        a.uexp_x = at<int>(ws, L.uctl);
+        a.amax = at<unsigned>(ws, L.uctl + 32);
+        a.uexp_h = at<int>(ws, L.uctl + 64);
+        a.zbuf = at<float>(ws, L.zbuf);
+        a.ucnt = at<unsigned>(ws, L.ucnt);
+        a.ctrl = at<WsCtrl>(ws, L.ctrl);
+        if (launch_pred_union(a, s) != cudaSuccess) return PI_ERR_CUDA;
+        if (launch_compact(a.mask, D->d_ff, idx, n_active, cap, a.ctrl, at<unsigned long long>(ws, L.status), s) !=
+            cudaSuccess)
+            return PI_ERR_CUDA;
+        if (y_init && launch_init_y(y_init, D->b_down, residual, B, D->d_model, nullptr, nullptr, 0, s) != cudaSuccess)
+            return PI_ERR_CUDA;
+        return PI_OK;
+    }
     float *h = at<float>(ws, L.h);
     const size_t p2_bytes = (size_t)D->d_ff * D->rank * (D->ptype == PI_F16 ? 2 : 4);
     cudaError_t e = launch_pred_hidden(D->ptype, D->p1, x, B, D->d_model, D->rank, h, D->p2, p2_bytes, D->p_bias,
@@ -161,7 +197,7 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
 }
 
 pi_status enqueue_sparse(const pi_ffn_desc *D, const float *x, int32_t B, const int32_t *idx,
-                         const int32_t *n_active, float *y, void *ws, cudaStream_t s)
+                         const int32_t *n_active, float *y, void *ws, cudaStream_t s, bool xf_ready = false)
 {
     const WsLayout L = ws_layout(D->d_model, D->d_ff, D->rank, B);
     SparseParams p{};
@@ -181,6 +217,7 @@ pi_status enqueue_sparse(const pi_ffn_desc *D, const float *x, int32_t B, const 
         p.amax = at<unsigned>(ws, L.uctl + 32);
         p.zbuf = at<float>(ws, L.zbuf);
         p.ucnt = at<unsigned>(ws, L.ucnt);
+        p.xf_ready = xf_ready ? 1 : 0;
     }
     p.d = D->d_model;
     p.F = D->d_ff;
@@ -316,7 +353,9 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
     }
     st = enqueue_predict(desc, x, batch, nullptr, nullptr, idx, n_active, desc->d_ff, ws, y, residual, s);
     if (st != PI_OK) return st;
-    return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s);
+    // the tensor-core predictor left x's fp16 fragments in the workspace (fp16 layout)
+    const bool xf_ready = batch > 1 && desc->ptype == PI_F16 && desc->wtype == PI_F16;
+    return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s, xf_ready);
 }
 
 pi_status pi_dense_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,

@@ -21,7 +21,9 @@ struct WsLayout {
     size_t fcount;    // one-kernel layer step: per-CTA active counts [1024] u32
     size_t act;       // union path: activations, [ceil(d_ff/16)][4][8][4] fp32 (mma B-operand order)
     size_t xf;        // union path: x as fp16 hi/lo mma fragments, [ceil(d_model/32)][2][32][4] u32
-    size_t uctl;      // union path: per-token exponents int[8], then max |a| bits u32[8]
+    size_t uctl;      // union path: x exponents int[8], max |a| bits u32[8], h exponents int[8]
+    size_t xfh;       // union path: h as fp16 hi/lo mma fragments, [ceil(rank/32)][2][32][4] u32
+    size_t umask;     // union path: predicted union mask bytes [d_ff]
     size_t zbuf;      // union path: per-tile partial sums [ceil(d_ff/16)][2][16][8] fp32 (kept zero)
     size_t ucnt;      // union path: per-tile arrival counts [ceil(d_ff/16)] u32 (kept zero)
     size_t total;
@@ -93,8 +95,35 @@ struct SparseParams {
     unsigned *amax;         // union path: per-token max |a| (float bits) [8]
     float *zbuf;            // union path: per-tile partial sums
     unsigned *ucnt;         // union path: per-tile arrival counts
+    int xf_ready;           // union path: xf already holds x's fragments (skip the prep kernel)
     int d, F, act, B;
+    // The same up kernel also runs the batched predictor (idx and n_active null:
+    // every row of w_act in order, F rows of d weights):
+    float *out_h;           // hidden epilogue: h [B][F]
+    const float *p_bias;    // logits epilogue
+    float tau;
+    float *out_logits;      // logits epilogue: [B][F] or null
+    uint8_t *out_mask;      // logits epilogue: union mask bytes [F]
 };
+
+// Batched (2..8 tokens) predictor on tensor cores, fp16 predictor weights.
+struct UnionPredArgs {
+    const void *p1, *p2;
+    const float *p_bias;
+    float tau;
+    const float *x;
+    int B, d, r, F;
+    float *h;               // [B][r]
+    float *logits;          // [B][F] or null
+    uint8_t *mask;          // [F]
+    uint32_t *xf_x, *xf_h;  // operand fragments of x and of h
+    int *uexp_x, *uexp_h;
+    unsigned *amax;
+    float *zbuf;
+    unsigned *ucnt;
+    WsCtrl *ctrl;
+};
+cudaError_t launch_pred_union(const UnionPredArgs &a, cudaStream_t s);
 
 cudaError_t launch_sparse_b1(int wtype, int gated, const SparseParams &p, cudaStream_t s);
 cudaError_t launch_sparse_union(int wtype, int gated, const SparseParams &p, cudaStream_t s);

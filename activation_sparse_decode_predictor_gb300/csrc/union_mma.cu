@@ -66,6 +66,7 @@ constexpr size_t kSmemBudget = 225 * 1024;
 constexpr int kScaleExp = 10;            // scaled operands have their maximum in [2^10, 2^11)
 constexpr int kBatchJobs = 8;            // producer reads idx for 8 jobs (128 rows) at a time
 constexpr int kSlots = 4;                // up kernel: partial-sum slots in flight
+constexpr int kEpiFfn = 0, kEpiHidden = 1, kEpiLogits = 2;  // up kernel epilogues
 
 // Up-projection chunks (weights of d_model per unit) and shared-memory row strides.
 constexpr int kKsF16 = 2048;
@@ -245,7 +246,7 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, int nstages,
             if (jj < cnt) {
                 int row = 16 * job_tile(jj) + (v & 15);
                 row = row < n ? row : n - 1;
-                out[i] = __ldcg(p.idx + row);
+                out[i] = p.idx ? __ldcg(p.idx + row) : row;
             }
         }
     };
@@ -319,7 +320,7 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, int nstages,
 }
 
 // ------------------------------------------------------------------------------------
-template <int WT, bool GATED, int NG>
+template <int WT, bool GATED, int NG, int EPI>
 __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int nstages)
 {
     constexpr bool Q4 = WT == PI_Q4_0;
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
     pdl_wait();
     pdl_trigger();
 
-    int n = __ldcg(p.n_active);
+    int n = p.n_active ? __ldcg(p.n_active) : F;  // no list: every row of W, in order
     n = n < 0 ? 0 : (n > F ? F : n);
     const int T = (n + 15) >> 4;
     const int C = (d + KS - 1) / KS;
@@ -372,6 +373,45 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
 #pragma unroll
         for (int i = 0; i < 4; ++i) rsc[i] = ldexpf(1.f, __ldcg(p.uexp + rtb + i));
         const int B = p.B;
+        float mx[4] = {0.f, 0.f, 0.f, 0.f};  // largest |a| per token (FFN epilogue)
+        // Epilogue of one finished 16-row tile for this lane's row and 4 tokens:
+        //   FFN:    a = act(z + b) (* u) -> activation fragments of the down kernel;
+        //   hidden: h = max(z, 0) -> h[token][row];
+        //   logits: l = z + p_bias -> logits (optional), union over tokens of l > tau -> mask.
+        auto epilogue = [&](int tile, float4 zg, float4 zu, float bias, bool valid) {
+            const int k = 16 * tile + rrow;
+            const float zgv[4] = {zg.x, zg.y, zg.z, zg.w};
+            const float zuv[4] = {zu.x, zu.y, zu.z, zu.w};
+            if constexpr (EPI == kEpiFfn) {
+                const int tq = (rrow & 7) >> 1, jx = (rrow & 1) + 2 * (rrow >> 3);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a = 0.f;
+                    if (valid && rtb + i < B) {
+                        a = activate(p.act, zgv[i] + bias);
+                        if constexpr (GATED) a *= zuv[i];
+                    }
+                    p.act_ws[(((size_t)tile * 8 + rtb + i) * 4 + tq) * 4 + jx] = a;
+                    mx[i] = fmaxf(mx[i], fabsf(a));
+                }
+            } else if constexpr (EPI == kEpiHidden) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (valid && rtb + i < B) p.out_h[(size_t)(rtb + i) * F + k] = fmaxf(zgv[i], 0.f);
+            } else {
+                bool on = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (valid && rtb + i < B) {
+                        const float l = zgv[i] + bias;
+                        if (p.out_logits) p.out_logits[(size_t)(rtb + i) * F + k] = l;
+                        on = on || l > p.tau;
+                    }
+                const int other = __shfl_xor_sync(0xffffffffu, on ? 1 : 0, 1);  // the row's other 4 tokens
+                on = on || other != 0;
+                if (valid && rtb == 0) p.out_mask[k] = on ? 1 : 0;
+            }
+        };
         for (int jn = 0; jn < cnt;) {
             int nb = 0;
             for (; nb < kSlots && jn + nb < cnt; ++nb) {
@@ -384,14 +424,15 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
             // now so their latency hides behind the atomics and the fence below
             int jid[kSlots];
             float bias[kSlots];
+            const float *bvec = EPI == kEpiFfn ? p.b_act : (EPI == kEpiLogits ? p.p_bias : nullptr);
 #pragma unroll
             for (int b = 0; b < kSlots; ++b) {
                 const int k = 16 * (((u0 + jn + b) % per) / M) + rrow;
-                jid[b] = (b < nb && k < n) ? __ldcg(p.idx + k) : -1;
+                jid[b] = (b < nb && k < n) ? (p.idx ? __ldcg(p.idx + k) : k) : -1;
             }
 #pragma unroll
             for (int b = 0; b < kSlots; ++b)
-                bias[b] = (jid[b] >= 0 && jid[b] < F && p.b_act) ? __ldg(p.b_act + jid[b]) : 0.f;
+                bias[b] = (jid[b] >= 0 && jid[b] < F && bvec) ? __ldg(bvec + jid[b]) : 0.f;
             for (int b = 0; b < nb; ++b) {
                 const int jj = jn + b, u = u0 + jj;
                 const float *rb = red + (size_t)(jj % kSlots) * (kUW * 128);
@@ -405,71 +446,64 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
                         v.z += pz.z;
                         v.w += pz.w;
                     }
-                }
-                mbar_arrive(&fre[jj % kSlots]);
-                if (NG == 2 || rtb == 0) {
                     v.x *= rsc[0];
                     v.y *= rsc[1];
                     v.z *= rsc[2];
                     v.w *= rsc[3];
-                    const int tile = (u % per) / M, m = u % M;
-                    atomicAdd(reinterpret_cast<float4 *>(p.zbuf + ((size_t)tile * 2 + m) * 128 + rrow * 8 + rtb), v);
+                }
+                mbar_arrive(&fre[jj % kSlots]);
+                const int tile = (u % per) / M;
+                if (C * M == 1) {
+                    // one unit is the whole tile: no partial sums to combine
+                    epilogue(tile, v, make_float4(0.f, 0.f, 0.f, 0.f), bias[b], jid[b] >= 0 && jid[b] < F);
+                } else if (NG == 2 || rtb == 0) {
+                    atomicAdd(reinterpret_cast<float4 *>(p.zbuf + ((size_t)tile * 2 + u % M) * 128 + rrow * 8 + rtb), v);
                 }
             }
-            fence_acq_rel_gpu();
-            __syncwarp();
-            unsigned old = 0;
-            if (lane < nb) old = atomicAdd(p.ucnt + ((u0 + jn + lane) % per) / M, 1u);
-            const unsigned last = __ballot_sync(0xffffffffu, lane < nb && old == (unsigned)(C * M - 1));
-            if (last) {
-                // ---- tiles completed by this batch: activation, fragment-order store, reset ----
+            if (C * M > 1) {
                 fence_acq_rel_gpu();
-                float4 zg[kSlots], zu[kSlots];
+                __syncwarp();
+                unsigned old = 0;
+                if (lane < nb) old = atomicAdd(p.ucnt + ((u0 + jn + lane) % per) / M, 1u);
+                const unsigned last = __ballot_sync(0xffffffffu, lane < nb && old == (unsigned)(C * M - 1));
+                if (last) {
+                    // ---- tiles completed by this batch: epilogue, then reset their buffers ----
+                    fence_acq_rel_gpu();
+                    float4 zg[kSlots], zu[kSlots];
 #pragma unroll
-                for (int b = 0; b < kSlots; ++b) {
-                    zg[b] = zu[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if ((last >> b) & 1u) {
-                        const float *zt = p.zbuf + (size_t)(((u0 + jn + b) % per) / M) * 256 + rrow * 8 + rtb;
-                        zg[b] = __ldcg(reinterpret_cast<const float4 *>(zt));
-                        if constexpr (GATED) zu[b] = __ldcg(reinterpret_cast<const float4 *>(zt + 128));
-                    }
-                }
-                float mx[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int b = 0; b < kSlots; ++b) {
-                    if (!((last >> b) & 1u)) continue;
-                    const int tile = ((u0 + jn + b) % per) / M;
-                    float *zt = p.zbuf + (size_t)tile * 256 + rrow * 8 + rtb;
-                    __stcg(reinterpret_cast<float4 *>(zt), make_float4(0.f, 0.f, 0.f, 0.f));
-                    if constexpr (GATED) __stcg(reinterpret_cast<float4 *>(zt + 128), make_float4(0.f, 0.f, 0.f, 0.f));
-                    // an out-of-range neuron id (flagged by the producer, which copied row 0
-                    // in its place) contributes nothing
-                    const bool valid = jid[b] >= 0 && jid[b] < F;
-                    const float zgv[4] = {zg[b].x, zg[b].y, zg[b].z, zg[b].w};
-                    const float zuv[4] = {zu[b].x, zu[b].y, zu[b].z, zu[b].w};
-                    const int tq = (rrow & 7) >> 1, jx = (rrow & 1) + 2 * (rrow >> 3);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float a = 0.f;
-                        if (valid && rtb + i < B) {
-                            a = activate(p.act, zgv[i] + bias[b]);
-                            if constexpr (GATED) a *= zuv[i];
+                    for (int b = 0; b < kSlots; ++b) {
+                        zg[b] = zu[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if ((last >> b) & 1u) {
+                            const float *zt = p.zbuf + (size_t)(((u0 + jn + b) % per) / M) * 256 + rrow * 8 + rtb;
+                            zg[b] = __ldcg(reinterpret_cast<const float4 *>(zt));
+                            if constexpr (GATED) zu[b] = __ldcg(reinterpret_cast<const float4 *>(zt + 128));
                         }
-                        p.act_ws[(((size_t)tile * 8 + rtb + i) * 4 + tq) * 4 + jx] = a;
-                        mx[i] = fmaxf(mx[i], fabsf(a));
                     }
-                    if (lane == b) p.ucnt[tile] = 0u;
+#pragma unroll
+                    for (int b = 0; b < kSlots; ++b) {
+                        if (!((last >> b) & 1u)) continue;
+                        const int tile = ((u0 + jn + b) % per) / M;
+                        float *zt = p.zbuf + (size_t)tile * 256 + rrow * 8 + rtb;
+                        __stcg(reinterpret_cast<float4 *>(zt), make_float4(0.f, 0.f, 0.f, 0.f));
+                        if constexpr (GATED) __stcg(reinterpret_cast<float4 *>(zt + 128), make_float4(0.f, 0.f, 0.f, 0.f));
+                        // an out-of-range neuron id (flagged by the producer, which copied
+                        // row 0 in its place) contributes nothing
+                        epilogue(tile, zg[b], zu[b], bias[b], jid[b] >= 0 && jid[b] < F);
+                        if (lane == b) p.ucnt[tile] = 0u;
+                    }
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int o = 2; o < 32; o <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], o));
-                if (lane < 2)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (mx[i] > 0.f) atomicMax(p.amax + rtb + i, __float_as_uint(mx[i]));
             }
             jn += nb;
+        }
+        if constexpr (EPI == kEpiFfn) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int o = 2; o < 32; o <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], o));
+            if (lane < 2)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (mx[i] > 0.f) atomicMax(p.amax + rtb + i, __float_as_uint(mx[i]));
         }
         return;
     }
@@ -831,7 +865,7 @@ cudaError_t set_smem(K kern, size_t bytes)
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int WT, bool GATED, int NG>
+template <int WT, bool GATED, int NG, int EPI = kEpiFfn>
 cudaError_t launch_up(const SparseParams &p, cudaStream_t s)
 {
     constexpr uint32_t SB = up_stage_bytes(WT == PI_Q4_0);
@@ -841,11 +875,11 @@ cudaError_t launch_up(const SparseParams &p, cudaStream_t s)
     const size_t smem = kHdrU + (size_t)ns * SB + rbytes;
     static bool once = false;
     if (!once) {
-        cudaError_t e = set_smem(k_union_up<WT, GATED, NG>, smem);
+        cudaError_t e = set_smem(k_union_up<WT, GATED, NG, EPI>, smem);
         if (e != cudaSuccess) return e;
         once = true;
     }
-    return launch_pdl(k_union_up<WT, GATED, NG>, dim3(sm_count()), dim3(kUpThreads), smem, s, p, ns);
+    return launch_pdl(k_union_up<WT, GATED, NG, EPI>, dim3(sm_count()), dim3(kUpThreads), smem, s, p, ns);
 }
 
 template <int WT, int NG>
@@ -884,10 +918,50 @@ cudaError_t launch_sparse_union(int wtype, int gated, const SparseParams &p, cud
 {
     if (wtype != PI_F16 && wtype != PI_Q4_0) return cudaErrorNotSupported;
     if (p.B < 2 || p.B > 8) return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(k_union_prep, dim3(8, kPrepSplit), dim3(256), 0, s, p.x, p.B, p.d, wtype == PI_Q4_0 ? 1 : 0,
-                               p.xf, p.uexp, p.amax);
-    if (e != cudaSuccess) return e;
+    if (!p.xf_ready) {
+        const cudaError_t e = launch_pdl(k_union_prep, dim3(8, kPrepSplit), dim3(256), 0, s, p.x, p.B, p.d,
+                                         wtype == PI_Q4_0 ? 1 : 0, p.xf, p.uexp, p.amax);
+        if (e != cudaSuccess) return e;
+    }
     return wtype == PI_Q4_0 ? launch_union_wt<PI_Q4_0>(gated, p, s) : launch_union_wt<PI_F16>(gated, p, s);
+}
+
+cudaError_t launch_pred_union(const UnionPredArgs &a, cudaStream_t s)
+{
+    if (a.B < 2 || a.B > 8) return cudaErrorInvalidValue;
+    // x -> fragments (these also serve the FFN's up projection, which is told to skip its own)
+    cudaError_t e = launch_pdl(k_union_prep, dim3(8, kPrepSplit), dim3(256), 0, s, a.x, a.B, a.d, 0, a.xf_x, a.uexp_x,
+                               a.amax);
+    if (e != cudaSuccess) return e;
+    SparseParams q{};
+    q.ctrl = a.ctrl;
+    q.zbuf = a.zbuf;
+    q.ucnt = a.ucnt;
+    q.B = a.B;
+    q.act = 0;
+    // h = max(P1 x, 0): every row of P1 against the tokens
+    q.w_act = static_cast<const uint8_t *>(a.p1);
+    q.xf = a.xf_x;
+    q.uexp = a.uexp_x;
+    q.d = a.d;
+    q.F = a.r;
+    q.out_h = a.h;
+    e = a.B > 4 ? launch_up<PI_F16, false, 2, kEpiHidden>(q, s) : launch_up<PI_F16, false, 1, kEpiHidden>(q, s);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_union_prep, dim3(8, kPrepSplit), dim3(256), 0, s, a.h, a.B, a.r, 0, a.xf_h, a.uexp_h, a.amax);
+    if (e != cudaSuccess) return e;
+    // logits = P2 h + p_bias, union over tokens of logit > tau -> mask
+    q.w_act = static_cast<const uint8_t *>(a.p2);
+    q.xf = a.xf_h;
+    q.uexp = a.uexp_h;
+    q.d = a.r;
+    q.F = a.F;
+    q.out_h = nullptr;
+    q.p_bias = a.p_bias;
+    q.tau = a.tau;
+    q.out_logits = a.logits;
+    q.out_mask = a.mask;
+    return a.B > 4 ? launch_up<PI_F16, false, 2, kEpiLogits>(q, s) : launch_up<PI_F16, false, 1, kEpiLogits>(q, s);
 }
 
 }  // namespace pi
