@@ -30,9 +30,10 @@
 //      producer (an mbarrier), which asks L2 for all their rows at once and
 //      then runs the FFN jobs as sparse_ffn.cu does; the CTA's partial output
 //      goes to y with 16-byte vector atomics.
-// The grid barriers are counter barriers: one thread per CTA arrives with an
-// atomic add; the last arrival resets the counter and moves a generation word
-// on, which the other CTAs' single thread polls (bounded).
+// The grid barriers are counter barriers: one thread per CTA arrives with a
+// release add on a 64-bit counter that is never reset and polls it (acquire,
+// bounded) until it reaches a target derived from a per-launch sequence
+// number, so no arrival ever has to reset anything.
 #include <algorithm>
 
 #include "ffn_rows.cuh"

@@ -406,6 +406,85 @@ __global__ void __launch_bounds__(kCThreads, 1) k_compact(const uint8_t *__restr
     scan_finish(ctrl, G, epoch);
 }
 
+// The same compaction for masks of at most 64 Ki entries in one CTA.  Warp w owns
+// bytes [2048 w, 2048 w + 2048) as 16 rounds of 128 bytes (lane l: bytes 4l..4l+3
+// of the round), all loaded up front.  The warp totals are scanned across the
+// block; then, round by round, a shuffle scan of the lanes' counts gives each
+// lane its output slots, so a round's indices leave as one contiguous run.  No
+// cross-CTA wait at all.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallMax = 2048 * (kSmallThreads / 32);
+
+__global__ void __launch_bounds__(kSmallThreads, 1) k_compact_small(const uint8_t *__restrict__ mask, int n, int *idx,
+                                                                    int *count_out, int cap, unsigned *err)
+{
+    __shared__ unsigned wsum[kSmallThreads / 32];
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned nib[16];  // per round: bit e set if byte 4 lane + e of the round is non-zero
+    unsigned mine = 0;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const int o = 2048 * warp + 128 * r + 4 * lane;
+        unsigned w = 0;
+        if (o + 4 <= n) {
+            w = *reinterpret_cast<const unsigned *>(mask + o);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (o + e < n) w |= (unsigned)mask[o + e] << (8 * e);
+        }
+        nib[r] = ((w & 0xffu) ? 1u : 0u) | ((w & 0xff00u) ? 2u : 0u) | ((w & 0xff0000u) ? 4u : 0u) |
+                 ((w & 0xff000000u) ? 8u : 0u);
+        mine += __popc(nib[r]);
+    }
+    unsigned tot = mine;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane == 0) wsum[warp] = tot;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned x = wsum[lane];
+        unsigned xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, xi, o);
+            if (lane >= o) xi += y;
+        }
+        wsum[lane] = xi - x;  // exclusive over warps
+        if (lane == 31) {
+            unsigned all = xi;
+            if (all > (unsigned)cap) {
+                atomicOr(err, ERR_CAPACITY);
+                all = (unsigned)cap;
+            }
+            *count_out = (int)all;
+        }
+    }
+    __syncthreads();
+    unsigned base = wsum[warp];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const unsigned c = __popc(nib[r]);
+        unsigned incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        unsigned pos = base + incl - c;
+        const int b0 = 2048 * warp + 128 * r + 4 * lane;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if ((nib[r] >> e) & 1u) {
+                if (pos < (unsigned)cap) idx[pos] = b0 + e;
+                ++pos;
+            }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------------
@@ -459,6 +538,8 @@ cudaError_t launch_pred_logits(int ptype, const PredParams &p, cudaStream_t s)
 cudaError_t launch_compact(const uint8_t *mask, int n, int *idx, int *count, int cap, WsCtrl *ctrl,
                            unsigned long long *status, cudaStream_t s)
 {
+    if (n <= kSmallMax && ((uintptr_t)mask & 3) == 0)
+        return launch_pdl(k_compact_small, dim3(1), dim3(kSmallThreads), 0, s, mask, n, idx, count, cap, &ctrl->err);
     const int G = scan_grid(n);
     const int nw = ((n + G - 1) / G + 31) / 32 + 1;
     const size_t smem = (size_t)2 * nw * sizeof(unsigned);

@@ -71,9 +71,6 @@ constexpr int kEpiFfn = 0, kEpiHidden = 1, kEpiLogits = 2;  // up kernel epilogu
 // Up-projection chunks (weights of d_model per unit) and shared-memory row strides.
 constexpr int kKsF16 = 2048;
 constexpr int kKsQ4 = 4096;
-constexpr int kRsF16Up = kKsF16 * 2 + 64;  // 4160: 16-byte row reads of 8 lanes hit distinct banks
-constexpr int kRsQ4Up = kKsQ4 / 2 + 16;    // 2064: 32-bit row reads conflict-free
-constexpr int kSsQ4Up = kKsQ4 / 16 + 16;   // 272: scale rows on distinct banks
 // Down-projection column blocks.
 constexpr int kCw = 2048;                  // columns per block (4 KB fp16 row pieces)
 constexpr int kWc = kCw / kUW;             // 256 columns per consumer warp
@@ -84,7 +81,6 @@ constexpr int kSsQ4Dn = kCw / 16 + 16;     // 144
 constexpr int kFlushCols = 64;             // columns per pass of the down kernel's flush
 constexpr uint32_t kTileAct = 512;         // activations of one 16-row tile: [8 tokens][4][4] fp32
 
-constexpr uint32_t up_stage_bytes(bool q4) { return q4 ? 16u * (kRsQ4Up + kSsQ4Up) : 16u * kRsF16Up; }
 constexpr uint32_t dn_act_off(bool q4) { return q4 ? 16u * (kRsQ4Dn + kSsQ4Dn) : 16u * kRsF16Dn; }
 constexpr uint32_t dn_stage_bytes(bool q4) { return dn_act_off(q4) + kTileAct; }
 
@@ -321,13 +317,13 @@ __device__ void produce_rows(const SparseParams &p, int n, int cnt, int nstages,
 
 // ------------------------------------------------------------------------------------
 template <int WT, bool GATED, int NG, int EPI>
-__global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int nstages)
+__global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int nstages, int rs, int ss, uint32_t SB)
 {
     constexpr bool Q4 = WT == PI_Q4_0;
     constexpr int KS = Q4 ? kKsQ4 : kKsF16;   // weights of d_model per unit
     constexpr int SPW = KS / 32 / kUW;        // 32-wide steps per warp and unit
     constexpr int M = GATED ? 2 : 1;          // matrices per row tile
-    constexpr uint32_t SB = up_stage_bytes(Q4);
+    // rs, ss: row strides of a stage (code / fp16 rows; Q4_0 scale rows), SB: stage bytes
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kUMaxStages;
@@ -433,7 +429,9 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
 #pragma unroll
             for (int b = 0; b < kSlots; ++b)
                 bias[b] = (jid[b] >= 0 && jid[b] < F && bvec) ? __ldg(bvec + jid[b]) : 0.f;
-            for (int b = 0; b < nb; ++b) {
+#pragma unroll
+            for (int b = 0; b < kSlots; ++b) {
+                if (b >= nb) break;
                 const int jj = jn + b, u = u0 + jj;
                 const float *rb = red + (size_t)(jj % kSlots) * (kUW * 128);
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -523,11 +521,11 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
             uint8_t *st = stages + (size_t)s * SB;
             const size_t jn = (size_t)rows[lane];
             if constexpr (Q4) {
-                bulk_g2s(st + lane * kRsQ4Up, W + jn * (d / 2) + k0 / 2, (uint32_t)(len / 2), &full[s]);
-                bulk_g2s(st + 16 * kRsQ4Up + lane * kSsQ4Up, W + (size_t)F * (d / 2) + jn * (d / 16) + k0 / 16,
+                bulk_g2s(st + lane * rs, W + jn * (d / 2) + k0 / 2, (uint32_t)(len / 2), &full[s]);
+                bulk_g2s(st + 16 * rs + lane * ss, W + (size_t)F * (d / 2) + jn * (d / 16) + k0 / 16,
                          (uint32_t)(len / 16), &full[s]);
             } else {
-                bulk_g2s(st + lane * kRsF16Up, W + (jn * d + k0) * 2, (uint32_t)len * 2u, &full[s]);
+                bulk_g2s(st + lane * rs, W + (jn * d + k0) * 2, (uint32_t)len * 2u, &full[s]);
             }
         };
         produce_rows(p, n, cnt, nstages, 0, 0u, full, empty, tab, job_tile, job_bytes, issue, [](int, int) {});
@@ -566,8 +564,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
         const int q1 = min(q0 + SPW, (len + 31) / 32);
         const uint8_t *xfp = reinterpret_cast<const uint8_t *>(p.xf) + ((size_t)(k0 / 32) * NG * 32 + lane) * 16;
         if constexpr (!Q4) {
-            const uint8_t *ra = st + g * kRsF16Up + 16 * t;
-            const uint8_t *rb = ra + 8 * kRsF16Up;
+            const uint8_t *ra = st + g * rs + 16 * t;
+            const uint8_t *rb = ra + 8 * rs;
 #pragma unroll
             for (int i = 0; i < SPW; ++i) {
                 const int q = q0 + i;
@@ -584,10 +582,10 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
                 }
             }
         } else {
-            const uint8_t *ca = st + g * kRsQ4Up + 4 * t;
-            const uint8_t *cb = ca + 8 * kRsQ4Up;
-            const __half *sa = reinterpret_cast<const __half *>(st + 16 * kRsQ4Up + g * kSsQ4Up);
-            const __half *sb = reinterpret_cast<const __half *>(st + 16 * kRsQ4Up + (g + 8) * kSsQ4Up);
+            const uint8_t *ca = st + g * rs + 4 * t;
+            const uint8_t *cb = ca + 8 * rs;
+            const __half *sa = reinterpret_cast<const __half *>(st + 16 * rs + g * ss);
+            const __half *sb = reinterpret_cast<const __half *>(st + 16 * rs + (g + 8) * ss);
 #pragma unroll
             for (int i = 0; i < SPW; ++i) {
                 const int q = q0 + i;
@@ -868,18 +866,31 @@ cudaError_t set_smem(K kern, size_t bytes)
 template <int WT, bool GATED, int NG, int EPI = kEpiFfn>
 cudaError_t launch_up(const SparseParams &p, cudaStream_t s)
 {
-    constexpr uint32_t SB = up_stage_bytes(WT == PI_Q4_0);
+    // stages sized by the widest chunk this contraction has (its K may be far below KS)
+    constexpr bool Q4 = WT == PI_Q4_0;
+    constexpr int KS = Q4 ? kKsQ4 : kKsF16;
+    const int kse = p.d < KS ? p.d : KS;
+    int rs, ss;
+    if (Q4) {
+        rs = kse / 2 + 16;   // kse % 256 == 0: rows 16 bytes past a 128-byte multiple
+        ss = kse / 16 + 16;
+    } else {
+        rs = (kse * 2 + 127) / 128 * 128 + 64;  // 64 bytes past a 128-byte multiple
+        ss = 0;
+    }
+    const uint32_t SB = 16u * (uint32_t)(rs + ss);
     constexpr size_t rbytes = (size_t)kSlots * kUW * 128 * 4;  // the partial-sum slots
     const size_t fit = (kSmemBudget - kHdrU - rbytes) / SB;
     const int ns = (int)(fit < (size_t)kUMaxStages ? fit : (size_t)kUMaxStages);
     const size_t smem = kHdrU + (size_t)ns * SB + rbytes;
     static bool once = false;
     if (!once) {
-        cudaError_t e = set_smem(k_union_up<WT, GATED, NG, EPI>, smem);
+        // the largest request any shape makes
+        cudaError_t e = set_smem(k_union_up<WT, GATED, NG, EPI>, kSmemBudget);
         if (e != cudaSuccess) return e;
         once = true;
     }
-    return launch_pdl(k_union_up<WT, GATED, NG, EPI>, dim3(sm_count()), dim3(kUpThreads), smem, s, p, ns);
+    return launch_pdl(k_union_up<WT, GATED, NG, EPI>, dim3(sm_count()), dim3(kUpThreads), smem, s, p, ns, rs, ss, SB);
 }
 
 template <int WT, int NG>

@@ -142,6 +142,21 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def job_time(ms_step, world, device):
+    """Time per step of the whole job: the slowest rank's (every rank calls this)."""
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([float(ms_step)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    return ms_step
+
+
+def whole_job_us_per_token(ms_step, tokens_per_rank, world):
+    """All ranks' tokens processed in the slowest rank's time (weak scaling)."""
+    return ms_step * 1000.0 / (tokens_per_rank * world)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -360,13 +375,8 @@ def run_ours(args, w):
     g_step = capture(step, stream)
     with Clocks(dev) as clk:
         ms = time_graph(g_step, args.steps, args.warmup, stream, barrier)
-    ms_step = ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=X.device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    us_tok = ms_step * 1000.0 / (T * world)          # whole job: all ranks' tokens in the max time
+    ms_step = job_time(ms / args.steps, world, X.device)
+    us_tok = whole_job_us_per_token(ms_step, T, world)
 
     peak, peak_src = measured_peaks()
     if args.quick:

@@ -48,3 +48,23 @@ def test_compact_capacity_overflow():
     assert st == 5                       # PI_ERR_CAPACITY
     assert cnt == cap
     assert np.array_equal(idx, ref[:cap])
+
+
+@pytest.mark.parametrize("n", [1000, 65536, 65537])
+@pytest.mark.parametrize("offset", [0, 4, 3])
+def test_compact_both_paths(n, offset):
+    """Masks of at most 64 Ki entries at a 4-byte-aligned address take the
+    one-CTA scan; a misaligned mask or a longer one takes the multi-CTA scan.
+    Both give the oracle's list."""
+    rng = np.random.default_rng(n + offset)
+    m = (rng.random(n) < 0.3).astype(np.uint8)
+    buf = torch.zeros(n + 16, dtype=torch.uint8, device="cuda")
+    buf[offset:offset + n] = torch.from_numpy(m).cuda()
+    mask = buf[offset:offset + n]
+    idx = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ws = B.pi_compact(mask, idx, cnt, cap=n)
+    assert B.pi_sync_status(ws) == B.PI_OK
+    ref = oracle.compact(m)
+    assert int(cnt.item()) == ref.size
+    assert np.array_equal(idx.cpu().numpy()[: ref.size], ref)
