@@ -81,8 +81,8 @@ constexpr int kSsQ4Dn = kCw / 16 + 16;     // 144
 constexpr int kFlushCols = 64;             // columns per pass of the down kernel's flush
 constexpr uint32_t kTileAct = 512;         // activations of one 16-row tile: [8 tokens][4][4] fp32
 
-constexpr uint32_t dn_act_off(bool q4) { return q4 ? 16u * (kRsQ4Dn + kSsQ4Dn) : 16u * kRsF16Dn; }
-constexpr uint32_t dn_stage_bytes(bool q4) { return dn_act_off(q4) + kTileAct; }
+__host__ __device__ constexpr uint32_t dn_act_off(bool q4) { return q4 ? 16u * (kRsQ4Dn + kSsQ4Dn) : 16u * kRsF16Dn; }
+__host__ __device__ constexpr uint32_t dn_stage_bytes(bool q4) { return dn_act_off(q4) + kTileAct; }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
     for (int jj = 0; jj < cnt; ++jj) {
         const int s = jj % nstages;
         const long long u = u0 + jj;
-        const int cb = (int)(u / T), tile = (int)(u % T);
+        const int cb = (int)(u / T);
         if (cb != cur) {
             if (cur >= 0) {
                 flush(cur);
