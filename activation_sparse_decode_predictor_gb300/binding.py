@@ -45,7 +45,8 @@ class FFNDesc(ctypes.Structure):
                 ("ptype", ctypes.c_int32), ("threshold", ctypes.c_float),
                 ("w_up", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("b_act", ctypes.c_void_p), ("b_down", ctypes.c_void_p),
-                ("p1", ctypes.c_void_p), ("p2", ctypes.c_void_p), ("p_bias", ctypes.c_void_p)]
+                ("p1", ctypes.c_void_p), ("p2", ctypes.c_void_p), ("p_bias", ctypes.c_void_p),
+                ("next", ctypes.c_void_p)]
 
 
 _lib = None
@@ -148,6 +149,12 @@ class Layer:
         self.desc = FFNDesc(self.d_model, self.d_ff, self.rank, int(self.gated), int(act), int(wtype), int(ptype),
                             float(threshold), _p(w_up), _p(w_gate), _p(w_down), _p(b_act), _p(b_down), _p(p1),
                             _p(p2), _p(p_bias))
+
+    def set_next(self, other: "Layer | None"):
+        """Name the layer run next on the same stream (its predictor weights are
+        asked into L2 during this layer's FFN phase), or None."""
+        self._next = other
+        self.desc.next = ctypes.addressof(other.desc) if other is not None else None
 
     @classmethod
     def from_dict(cls, L: dict, act=PI_ACT_RELU, threshold=None):

@@ -146,6 +146,8 @@ struct LayerB1Args {
     unsigned *status;       // [#SMs] workspace
     WsCtrl *ctrl;
     int d, F;
+    const void *pf[2];      // regions asked into L2 during the FFN phase (the next layer's P1), or null
+    size_t pf_bytes[2];
 };
 bool fused_layer_supported(int wtype, int ptype, int d, int F, int r);
 cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s);

@@ -145,6 +145,8 @@ struct FusedParams {
     WsCtrl *ctrl;
     int d, F, r, act;
     float tau;
+    const uint8_t *pf[2];  // the next layer's predictor weights (or null), asked into L2
+    size_t pf_bytes[2];
 };
 
 // Default: one CTA per SM with a deep ring.  With PI_FUSED_COLOCATE, narrow
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             }
             volatile int *state = T.state;
             int up = 0, ds = 0;
+            bool pf_done = false;
             while (!failed) {
                 int kind, i = 0, j = 0;
                 if (ds < up && state[ds] != 0) {
@@ -311,6 +314,19 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     mbar_arrive(&T.full[s]);
                 }
                 ++q;
+                if (!pf_done && up >= sn) {
+                    // every up row of the share is requested: while the rest of the
+                    // FFN phase runs on them, ask L2 for this CTA's slice of the
+                    // next layer's P1 (the next kernel's first phase waits on it)
+                    pf_done = true;
+                    for (int k = 0; k < 2; ++k) {
+                        if (!p.pf[k] || p.pf_bytes[k] == 0) continue;
+                        const size_t per = ((p.pf_bytes[k] + G - 1) / G + 15) & ~(size_t)15;
+                        const size_t off = (size_t)c * per;
+                        if (off < p.pf_bytes[k])
+                            prefetch_l2(p.pf[k] + off, (uint32_t)min(per, p.pf_bytes[k] - off));
+                    }
+                }
                 if (kind == kJobEnd) break;
             }
             if (failed) {  // never leave bulk copies in flight into this CTA's shared memory
@@ -736,6 +752,10 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     p.r = a.r;
     p.act = a.act;
     p.tau = a.tau;
+    for (int k = 0; k < 2; ++k) {
+        p.pf[k] = static_cast<const uint8_t *>(a.pf[k]);
+        p.pf_bytes[k] = a.pf[k] ? a.pf_bytes[k] : 0;
+    }
     const int esz = a.ptype == 1 ? 2 : 4;
     const uint32_t R = row_slot_bytes(a.wtype, a.d);
     uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});

@@ -103,7 +103,7 @@ typedef void *pi_stream; /* cudaStream_t */
  *   8 <= rank <= PI_MAX_RANK, rank % 8 == 0 (only checked by calls that run
  *   the predictor).
  */
-typedef struct {
+typedef struct pi_ffn_desc_s {
     int32_t d_model;
     int32_t d_ff;
     int32_t rank;
@@ -120,6 +120,13 @@ typedef struct {
     const void *p1;
     const void *p2;
     const float *p_bias;
+    /* Optional (NULL: none): the layer the caller runs next on the same stream.
+     * pi_ffn_layer at batch 1 asks L2 for that layer's predictor P1 while its
+     * own sparse FFN phase runs, so the next call's first phase finds it on
+     * chip; only the host reads *next (pointers and shape; a P1 not 16-byte
+     * aligned is skipped).  Layer-by-layer decode knows its next layer; the
+     * weights are still read from HBM once. */
+    const struct pi_ffn_desc_s *next;
 } pi_ffn_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */

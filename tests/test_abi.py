@@ -47,7 +47,8 @@ def test_status_strings(L):
 
 def _desc(**kw):
     d = dict(d_model=512, d_ff=2048, rank=64, gated=0, act=0, wtype=B.PI_F16, ptype=B.PI_F16, threshold=0.0,
-             w_up=0x1000, w_gate=None, w_down=0x2000, b_act=None, b_down=None, p1=0x3000, p2=0x4000, p_bias=None)
+             w_up=0x1000, w_gate=None, w_down=0x2000, b_act=None, b_down=None, p1=0x3000, p2=0x4000, p_bias=None,
+             next=None)
     d.update(kw)
     return B.FFNDesc(*[d[f] for f, _ in B.FFNDesc._fields_])
 

@@ -337,3 +337,29 @@ def test_layer_and_predict_share_a_workspace():
         assert B.pi_sync_status(ws) == 0
         got = set(idx.cpu().numpy()[: int(n.item())].tolist())
         assert all(amb[j] for j in got ^ ref)
+
+
+def test_next_layer_prefetch_changes_nothing():
+    """Naming the next layer only asks L2 for its predictor weights: outputs and
+    active lists stay those of the oracle, including with a misaligned (so not
+    prefetched) or self-referencing next layer."""
+    d, F, r = 512, 3000, 64
+    lay, olay, H = _layer(d, F, r, True, "f16", seed=97)
+    lay2, _, _ = _layer(d, F, r, False, "f16", seed=98)
+    X = synth.tokens(3, d, 99).numpy()
+    for nxt in (lay2, lay, None):
+        lay.set_next(nxt)
+        idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y = torch.empty(d, dtype=torch.float32, device="cuda")
+        ws = None
+        for t in range(X.shape[0]):
+            ws = B.pi_ffn_layer(lay, _cuda(X[t]), y, idx=idx, n_active=n, ws=ws)
+            assert B.pi_sync_status(ws) == 0
+            h, logit_ref, M = oracle.predict(olay, X[t])
+            amb = ambiguous(logit_ref, logit_scale(H, h), olay.threshold)
+            got, ref = set(idx.cpu().numpy()[: int(n.item())].tolist()), set(np.flatnonzero(M).tolist())
+            assert all(amb[j] for j in got ^ ref)
+            res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))), np.int32)
+            assert_ffn_close(y.cpu().numpy(), oracle.sparse_ffn(olay, X[t], res), what=f"next={nxt is not None} t={t}")
+    lay.set_next(None)
