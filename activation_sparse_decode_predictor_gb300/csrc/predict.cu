@@ -413,7 +413,8 @@ __global__ void __launch_bounds__(kCThreads, 1) k_compact(const uint8_t *__restr
 // lane its output slots, so a round's indices leave as one contiguous run.  No
 // cross-CTA wait at all.
 constexpr int kSmallThreads = 1024;
-constexpr int kSmallMax = 2048 * (kSmallThreads / 32);
+constexpr int kSmallMax = 2048 * (kSmallThreads / 32);  // capacity of the kernel
+constexpr int kSmallUse = 8192;  // used up to here: beyond, the multi-CTA scan measured faster (GB300)
 
 __global__ void __launch_bounds__(kSmallThreads, 1) k_compact_small(const uint8_t *__restrict__ mask, int n, int *idx,
                                                                     int *count_out, int cap, unsigned *err)
@@ -538,7 +539,7 @@ cudaError_t launch_pred_logits(int ptype, const PredParams &p, cudaStream_t s)
 cudaError_t launch_compact(const uint8_t *mask, int n, int *idx, int *count, int cap, WsCtrl *ctrl,
                            unsigned long long *status, cudaStream_t s)
 {
-    if (n <= kSmallMax && ((uintptr_t)mask & 3) == 0)
+    if (n <= kSmallUse && n <= kSmallMax && ((uintptr_t)mask & 3) == 0)
         return launch_pdl(k_compact_small, dim3(1), dim3(kSmallThreads), 0, s, mask, n, idx, count, cap, &ctrl->err);
     const int G = scan_grid(n);
     const int nw = ((n + G - 1) / G + 31) / 32 + 1;

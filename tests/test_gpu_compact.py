@@ -50,10 +50,10 @@ def test_compact_capacity_overflow():
     assert np.array_equal(idx, ref[:cap])
 
 
-@pytest.mark.parametrize("n", [1000, 65536, 65537])
+@pytest.mark.parametrize("n", [1000, 8192, 8193, 65537])
 @pytest.mark.parametrize("offset", [0, 4, 3])
 def test_compact_both_paths(n, offset):
-    """Masks of at most 64 Ki entries at a 4-byte-aligned address take the
+    """Masks of at most 8 Ki entries at a 4-byte-aligned address take the
     one-CTA scan; a misaligned mask or a longer one takes the multi-CTA scan.
     Both give the oracle's list."""
     rng = np.random.default_rng(n + offset)
