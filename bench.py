@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="decode tokens per step (default: the workload's)")
     ap.add_argument("--quick", action="store_true", help="main timed step only (for profiling runs)")
+    ap.add_argument("--one-layer", action="store_true",
+                    help="multi-layer workloads: time one layer on rotating copies instead of the stack")
     ap.add_argument("--batch", type=int, default=0,
                     help="tokens decoded together through the union path (default: the workload's)")
     return ap.parse_args()
@@ -308,12 +310,59 @@ def host_layer(L0, w=None):
 
 
 # ------------------------------------------------------------------------------------ arms
+def oracle_stack_sample(w, olays, X_host, budget_s):
+    """Time the oracle through every layer of a stack (predictor, compaction,
+    sparse FFN, residual + rescale) on as many tokens as fit the budget;
+    returns (us per layer per token, tokens)."""
+    import oracle
+    t0 = time.perf_counter()
+    done = 0
+    while done < X_host.shape[0] and (done == 0 or time.perf_counter() - t0 < budget_s):
+        xo = X_host[done]
+        for ol in olays:
+            _, _, m = oracle.predict(ol, xo)
+            yo = oracle.sparse_ffn(ol, xo, oracle.compact(m))
+            xo = oracle.rms_residual(xo, yo).astype(np.float32)
+        done += 1
+    return (time.perf_counter() - t0) / (done * len(olays)) * 1e6, done
+
+
+def oracle_layer(w, H):
+    import oracle
+    return oracle.Layer(w.d_model, w.d_ff, w.rank, H["w_up"], H["w_down"], w_gate=H["w_gate"], b_act=H["b_act"],
+                        b_down=H["b_down"], p1=H["p1"], p2=H["p2"], p_bias=H["p_bias"], threshold=H["threshold"])
+
+
 def run_reference(args, w):
     ws_, rank, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     oracle.build()
+    if w.layers > 1 and not args.one_layer:
+        olays = [oracle_layer(w, host_layer(synth.workload_layer(w, l, device="cpu"), w)) for l in range(w.layers)]
+        X = synth.workload_tokens(w, device="cpu").numpy()
+        per_step = []
+        budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+        ntok = 0
+        for s in range(args.warmup + args.steps):
+            us, ntok = oracle_stack_sample(w, olays, X[(s * 7) % X.shape[0]:], budget)
+            if s >= args.warmup:
+                per_step.append(us)
+        value = float(np.median(per_step))
+        line = {"impl": "reference", "metric": "us_per_ffn_layer_per_token", "value": value,
+                "unit": "us/layer/token", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": value * w.tokens * w.layers / 1000.0, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "d_model": w.d_model, "d_ff": w.d_ff, "rank": w.rank,
+                           "gated": w.gated, "weights": w.wtype, "batch": 1, "layers": w.layers,
+                           "sparsity": w.sparsity},
+                "cpu_baseline": {"value": value, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
+                                 "sample": f"{ntok} token(s) per step through all {w.layers} layers, "
+                                           "single-threaded C, fp64"},
+                "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
     L0 = synth.workload_layer(w, 0, device="cpu")
     H = host_layer(L0, w)
     X = synth.workload_tokens(w, device="cpu").numpy()
@@ -493,11 +542,144 @@ def run_ours(args, w):
     return 0
 
 
+def run_stack(args, w):
+    """Workloads of several layers (the OPT-175B-shaped stack): each token goes
+    through `w.layers` distinct layers, each layer's output plus its input
+    rescaled by pi_rms_residual into the next layer's input, and the whole token
+    is timed end to end.  Metric: us per layer per token (step time / tokens /
+    layers; the glue kernel is part of it)."""
+    world, rank, local = dist_env()
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        barrier = dist.barrier
+    dev = local
+    torch.cuda.set_device(dev)
+    B.lib()
+    nl = w.layers
+    Ls = [synth.workload_layer(w, l, device=f"cuda:{dev}") for l in range(nl)]
+    lays = [B.Layer.from_dict(L) for L in Ls]
+    for l in range(nl):
+        lays[l].set_next(lays[(l + 1) % nl])  # the next layer of the stack (layer 0 of the next token)
+    X = synth.workload_tokens(w, device=f"cuda:{dev}")
+    if args.tokens:
+        X = X[:args.tokens].contiguous()
+    T, d = X.shape
+    ws = B.workspace(B.pi_workspace_bytes(lays[0], 1), X.device)
+    ya = torch.empty(d, dtype=torch.float32, device=X.device)
+    bufs = [torch.empty(d, dtype=torch.float32, device=X.device) for _ in range(2)]
+    Xout = torch.empty(T, d, dtype=torch.float32, device=X.device)
+    stream = torch.cuda.Stream()
+
+    def token(xin, xout, record=None):
+        cur = xin
+        for l in range(nl):
+            if record is not None:
+                record[l].copy_(cur)
+            B.pi_ffn_layer(lays[l], cur, ya, ws=ws)
+            nxt = xout if l == nl - 1 else bufs[l % 2]
+            B.pi_rms_residual(cur, ya, nxt)
+            cur = nxt
+
+    def step(Xin=X):
+        for t in range(T):
+            token(Xin[t], Xout[t])
+
+    # statistics on the chained inputs of every layer (outside any timed region)
+    Xl = torch.empty(nl, T, d, dtype=torch.float32, device=X.device)
+    for t in range(T):
+        token(X[t], Xout[t], record=[Xl[l, t] for l in range(nl)])
+    torch.cuda.synchronize()
+    n_pred, n_down, recs, precs = [], [], [], []
+    for l in range(nl):
+        _, _, npl, ndl, rec, prec, _ = active_stats(w, Ls[l], lays[l], Xl[l], ws, ws, 1)
+        n_pred.append(npl)
+        n_down.append(ndl)
+        recs.append(rec)
+        precs.append(prec)
+    n_pred, n_down = np.concatenate(n_pred), np.concatenate(n_down)
+    pred_b, ffn_b = needed_bytes(w, n_pred, n_down, 1)
+    mean_bytes = float(np.mean(pred_b + ffn_b))  # per token and layer
+
+    g_step = capture(step, stream)
+    with Clocks(dev) as clk:
+        ms = time_graph(g_step, args.steps, args.warmup, stream, barrier)
+    ms_step = job_time(ms / args.steps, world, X.device)
+    us_tok = whole_job_us_per_token(ms_step, T * nl, world)  # per layer per token
+    layer_gbs = mean_bytes / (us_tok * world * 1e-6) / 1e9
+    peak, peak_src = measured_peaks()
+
+    # end to end: pinned host tokens in, the stack's outputs back
+    Xh = X.cpu().pin_memory()
+    Yh = torch.empty(T, d, dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(X)
+    e2e_steps = max(2, args.steps // 10)
+    with torch.cuda.stream(stream):
+        def e2e_step():
+            Xd.copy_(Xh, non_blocking=True)
+            step(Xd)
+            Yh.copy_(Xout, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    us_e2e = e0.elapsed_time(e1) / e2e_steps * 1000.0 / (T * nl)
+    st = B.pi_sync_status(ws)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        olays = [oracle_layer(w, host_layer(Ls[l], w)) for l in range(nl)]
+        us_cpu, done = oracle_stack_sample(w, olays, X.cpu().numpy(), args.cpu_seconds)
+        cpu = {"value": us_cpu, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
+               "sample": f"first {done} of {T} tokens through all {nl} layers (predictor, compaction, sparse FFN, "
+                         "residual + rescale), single-threaded C oracle, fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": "us_per_ffn_layer_per_token", "value": us_tok, "unit": "us/layer/token", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.wtype == "f16" else w.wtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "d_model": d, "d_ff": w.d_ff, "rank": w.rank, "gated": w.gated,
+                       "weights": w.wtype, "accumulate": "f32", "batch": 1, "layers": nl, "tokens_per_step": T,
+                       "sparsity": w.sparsity,
+                       "l2": f"inputs larger than L2: {nl} distinct layers, "
+                             f"{nl * mean_bytes / 1e6:.0f} MB needed bytes per token",
+                       "n_active_mean": float(np.mean(n_pred)), "n_nonzero_mean": float(np.mean(n_down)),
+                       "predictor_recall": float(np.mean(recs)), "predictor_precision": float(np.mean(precs)),
+                       "needed_bytes_per_token_layer": mean_bytes, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "k_layer_b1 (pi_ffn_layer; glue kernel included in the time)",
+                         "achieved": layer_gbs, "peak": peak, "unit": "GB/s", "frac": layer_gbs / peak,
+                         "traffic": None, "peak_source": peak_src},
+            "e2e": {"value": us_e2e, "unit": "us/layer/token", "h2d_bytes_per_step": int(Xh.numel() * 4),
+                    "d2h_bytes_per_step": int(Yh.numel() * 4), "path": "pi_ffn_layer + pi_rms_residual per layer"},
+            "gpu_launches": 2 * nl * T * args.steps,
+            "clocks": clk.summary(),
+            "device_status": st,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if w.layers > 1 and not args.one_layer:
+        return run_stack(args, w)
     return run_ours(args, w)
 
 

@@ -363,3 +363,18 @@ def test_next_layer_prefetch_changes_nothing():
             res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))), np.int32)
             assert_ffn_close(y.cpu().numpy(), oracle.sparse_ffn(olay, X[t], res), what=f"next={nxt is not None} t={t}")
     lay.set_next(None)
+
+
+@pytest.mark.parametrize("d", [8, 1030, 12288, 16384, 20000])
+def test_rms_residual_both_paths_and_in_place(d):
+    """16-byte aligned rows with d % 4 == 0 and d <= 16384 take the one-pass
+    vector kernel, the rest the strided one; out may alias x."""
+    rng = np.random.default_rng(d)
+    x = rng.standard_normal((3, d)).astype(np.float32)
+    y = rng.standard_normal((3, d)).astype(np.float32)
+    xd = _cuda(x)
+    B.pi_rms_residual(xd, _cuda(y), xd)          # in place
+    torch.cuda.synchronize()
+    for t in range(3):
+        np.testing.assert_allclose(xd[t].cpu().numpy(), oracle.rms_residual(x[t], y[t].astype(np.float64)),
+                                   rtol=1e-5, atol=1e-6)
