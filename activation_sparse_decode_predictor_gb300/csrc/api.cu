@@ -31,6 +31,8 @@ WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
     o = align256(o + 16);
     L.candb = o;
     if (batch == 1) o = align256(o + (size_t)d_ff * 4);
+    L.qent = o;
+    if (batch == 1) o = align256(o + (size_t)d_ff * 8);
     L.act = L.xf = L.uctl = L.zbuf = L.ucnt = L.xfh = L.umask = o;
     if (batch > 1) {
         const size_t tiles = ((size_t)d_ff + 15) / 16;
@@ -340,6 +342,7 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
         a.n_active = n_active;
         a.cand = at<int32_t>(ws, L.idx);
         a.cand_bias = at<float>(ws, L.candb);
+        a.qent = at<unsigned long long>(ws, L.qent);
         a.h = at<float>(ws, L.h);
         a.status = at<unsigned>(ws, L.fcount);
         a.ctrl = at<WsCtrl>(ws, L.ctrl);

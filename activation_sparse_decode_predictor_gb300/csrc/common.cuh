@@ -25,7 +25,10 @@ struct WsCtrl {
     unsigned epoch;         // scan: launch generation, tags the CTA status words
     unsigned long long bar_ctr;  // one-kernel layer step: grid-barrier arrivals (never reset)
     unsigned bar_seq;            // one-kernel layer step: launches completed (moves barrier targets)
-    unsigned pad[57];
+    unsigned q_head[2];          // one-kernel layer step, work queue (by launch parity): rows taken
+    unsigned q_tail[2];          //   rows reserved by publishing CTAs
+    unsigned q_done[2];          //   CTAs that have published all their rows
+    unsigned pad[51];
 };
 static_assert(sizeof(WsCtrl) == 256, "control block is 256 bytes");
 

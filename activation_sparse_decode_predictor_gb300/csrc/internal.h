@@ -18,6 +18,7 @@ struct WsLayout {
     size_t idx;       // internal active list [d_ff] int32
     size_t nact;      // internal active count (int32)
     size_t candb;     // one-kernel layer step: candidate biases [d_ff] fp32
+    size_t qent;      // one-kernel layer step: work-queue entries [d_ff] u64
     size_t fcount;    // one-kernel layer step: per-CTA active counts [1024] u32
     size_t act;       // union path: activations, [ceil(d_ff/16)][4][8][4] fp32 (mma B-operand order)
     size_t xf;        // union path: x as fp16 hi/lo mma fragments, [ceil(d_model/32)][2][32][4] u32
@@ -142,6 +143,7 @@ struct LayerB1Args {
     int *idx_out, *n_active;
     int *cand;              // [F] workspace
     float *cand_bias;       // [F] workspace
+    unsigned long long *qent;  // [F] workspace
     float *h;               // [r] workspace
     unsigned *status;       // [#SMs] workspace
     WsCtrl *ctrl;

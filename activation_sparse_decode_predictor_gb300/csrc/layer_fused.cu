@@ -55,6 +55,7 @@ constexpr int kGroup = 8;          // P2 rows per job
 constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
 constexpr int kUpRing = 32;        // FFN up rows in flight (> ring stages)
+constexpr int kQTake = 4;          // work-queue slots taken per atomic
 constexpr int kJobP1 = 1, kJobP2 = 2, kJobUp = 3, kJobDown = 4, kJobEnd = 5;
 
 struct Tables {
@@ -68,6 +69,7 @@ struct Tables {
     unsigned long long seq;
     int share_n;
     int count, total;
+    unsigned qbase;     // queue mode: this CTA's first reserved queue slot
     int wsum[kNCW];
     unsigned words[kMaxRange / 32 + 1];
     unsigned wpre[kMaxRange / 32 + 1];
@@ -95,6 +97,18 @@ __device__ __forceinline__ float ld_cg_f32(const float *p)
     float v;
     asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
     return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
@@ -140,6 +154,7 @@ struct FusedParams {
     int *n_active;       // or null
     int *cand;           // [F] candidate lists (each CTA writes inside its range)
     float *cand_bias;    // [F] b_act of each candidate
+    unsigned long long *qent;  // [F] work-queue entries: (launch sequence + 1) << 32 | neuron
     float *h;            // [rank]
     unsigned *status;    // [G] active count of each CTA's range
     WsCtrl *ctrl;
@@ -183,6 +198,11 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     const int rp1 = max(1, min(kMaxP1, (int)(stage_bytes / p1row)));  // P1 rows per job
     const int nP1 = (nP1r + rp1 - 1) / rp1;
     const int nP2 = (nR + kGroup - 1) / kGroup;
+    // No ordered active list requested: the FFN rows come from a shared work
+    // queue that every CTA feeds with its range's active neurons, so there is
+    // no second grid barrier, no prefix scan and no share lookup, and idle CTAs
+    // take rows from busy ones.
+    const bool qmode = !p.idx_out && !p.n_active;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
@@ -243,9 +263,11 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 }
                 ++q;
             }
-            // FFN jobs, once the consumers have found this CTA's share
+            // FFN jobs: with an ordered active list requested, once the consumers
+            // have found this CTA's share; otherwise (queue mode) from the shared
+            // work queue, once grid barrier A has reset it
             if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
-            const int sn = failed ? 0 : T.share_n;
+            int sn = (failed || qmode) ? 0 : T.share_n;
 #ifndef PI_FUSED_PREFETCH_DOWN
 #define PI_FUSED_PREFETCH_DOWN 0
 #endif
@@ -265,6 +287,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             volatile int *state = T.state;
             int up = 0, ds = 0;
             bool pf_done = false;
+            bool exhausted = !qmode;  // queue mode: more rows may still be published
+            int pend = -1, pk = 0;    // queue batch taken: slots [pend + pk, pend + kQTake) not read yet
+            long long qspins = 0;
+            const unsigned par = (unsigned)T.seq & 1u, tag = (unsigned)T.seq + 1u;
             while (!failed) {
                 int kind, i = 0, j = 0;
                 if (ds < up && state[ds] != 0) {
@@ -273,6 +299,57 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     if (stt == 1) continue;
                     kind = kJobDown;
                     j = T.j[i];
+                } else if (up >= sn && !exhausted) {
+                    // take kQTake queue slots with one atomic; read the batch's
+                    // remaining slots together; a slot is ready once its tag is
+                    // this launch's; a slot at or past the final tail ends the queue
+                    if (pend < 0) {
+                        if (sn >= kMaxShare) {
+                            exhausted = true;
+                            continue;
+                        }
+                        pend = (int)atomicAdd(&p.ctrl->q_head[par], (unsigned)kQTake);
+                        pk = 0;
+                        qspins = 0;
+                    }
+                    unsigned long long ev[kQTake];
+#pragma unroll
+                    for (int k = 0; k < kQTake; ++k) {
+                        const int slot = pend + pk + k;
+                        ev[k] = 0ull;
+                        if (pk + k < kQTake && slot < F)
+                            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(ev[k]) : "l"(p.qent + slot) : "memory");
+                    }
+                    int took = 0;
+#pragma unroll
+                    for (int k = 0; k < kQTake; ++k) {
+                        if (took != k || pk + k >= kQTake || sn >= kMaxShare) break;
+                        if ((unsigned)(ev[k] >> 32) != tag) break;
+                        T.j[sn++] = (int)(unsigned)(ev[k] & 0xffffffffull);
+                        ++took;
+                    }
+                    pk += took;
+                    if (pk == kQTake || sn >= kMaxShare) {
+                        pend = -1;
+                        continue;
+                    }
+                    if (took > 0) {
+                        qspins = 0;
+                        continue;  // issue those rows' jobs before looking again
+                    }
+                    if (ld_acquire_u32(&p.ctrl->q_done[par]) == (unsigned)G &&
+                        (unsigned)(pend + pk) >= ld_acquire_u32(&p.ctrl->q_tail[par])) {
+                        exhausted = true;  // every CTA has published: the tail is final
+                        pend = -1;
+                        continue;
+                    }
+                    if (++qspins < kSpinLimit) {
+                        __nanosleep(32);
+                        continue;
+                    }
+                    atomicOr(err, ERR_TIMEOUT);
+                    failed = true;
+                    kind = kJobEnd;
                 } else if (up < sn) {
                     i = up++;
                     j = T.j[i];
@@ -314,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     mbar_arrive(&T.full[s]);
                 }
                 ++q;
-                if (!pf_done && up >= sn) {
+                if (!pf_done && exhausted && up >= sn) {
                     // every up row of the share is requested: while the rest of the
                     // FFN phase runs on them, ask L2 for this CTA's slice of the
                     // next layer's P1 (the next kernel's first phase waits on it)
@@ -428,7 +505,20 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     // grid barrier A: every CTA's h slice and y initialisation are out
     named_bar_sync(1, kNCT);
     const unsigned long long base = (2ull * T.seq) * (unsigned long long)G;
+    const unsigned qpar = (unsigned)T.seq & 1u;
+    if (t == 0 && c == 0) {
+        // this launch's work-queue counters start from zero (nobody touches them
+        // before grid barrier A; the previous launch used the other set)
+        p.ctrl->q_head[qpar] = 0u;
+        p.ctrl->q_tail[qpar] = 0u;
+        p.ctrl->q_done[qpar] = 0u;
+    }
     if (t == 0 && !grid_barrier(&p.ctrl->bar_ctr, base + (unsigned long long)G, err)) ok = false;
+    if (t == 0) {
+        // every CTA has read this launch's sequence number: move it on
+        if (c == 0) atomicAdd(&p.ctrl->bar_seq, 1u);
+        if (qmode) mbar_arrive(&T.share_ready);  // the producer may take queue slots now
+    }
     named_bar_sync(1, kNCT);
     for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
     named_bar_sync(1, kNCT);
@@ -533,6 +623,29 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         if (t == 31) T.count = (int)inc;
     }
     named_bar_sync(1, kNCT);
+    if (qmode) {
+        // publish this range's active neurons as queue entries, count the CTA as
+        // published (release), and arrive at barrier B without waiting: the FFN
+        // takes its rows from the queue
+        if (t == 0) T.qbase = atomicAdd(&p.ctrl->q_tail[qpar], (unsigned)T.count);
+        named_bar_sync(1, kNCT);
+        const unsigned tag = (unsigned)T.seq + 1u;
+        for (int wd = warp; wd < nw; wd += kNCW) {
+            const unsigned bits = T.words[wd];
+            if ((bits >> lane) & 1u) {
+                const int pos = (int)T.qbase + (int)T.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
+                // tag and neuron in one 8-byte word: a reader that sees the tag sees the neuron
+                const unsigned long long e = ((unsigned long long)tag << 32) | (unsigned)(j0 + wd * 32 + lane);
+                asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.qent + pos), "l"(e) : "memory");
+            }
+        }
+        named_bar_sync(1, kNCT);
+        if (t == 0) {
+            __threadfence();
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.ctrl->q_done[qpar]) : "memory");
+            asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&p.ctrl->bar_ctr) : "memory");
+        }
+    } else {
     // candidate list of this range: ascending active neurons and their biases
     for (int wd = warp; wd < nw; wd += kNCW) {
         const unsigned bits = T.words[wd];
@@ -546,8 +659,6 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     if (t == 0) {
         p.status[c] = (unsigned)T.count;
         if (!grid_barrier(&p.ctrl->bar_ctr, base + 2ull * (unsigned long long)G, err)) ok = false;
-        // every CTA has read this launch's sequence number: move it on
-        if (c == 0) atomicAdd(&p.ctrl->bar_seq, 1u);
     }
     named_bar_sync(1, kNCT);
     // every range's count -> exclusive prefix and total
@@ -607,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         T.share_n = ok ? sn : 0;
         mbar_arrive(&T.share_ready);
     }
+    }  // ordered-list mode
 
     // ---- 3. the sparse FFN over this CTA's share ----
     bool any = false;
@@ -621,6 +733,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         const uint8_t *st = stages + (size_t)s * stage_bytes;
         if (job.x == kJobUp) {
+            // the row's bias: from the share table, or (queue mode) from b_act,
+            // loaded now and used by the warp that finishes the row
+            float bj = 0.f;
+            if (lane == 0) bj = qmode ? (p.b_act ? __ldg(p.b_act + job.z) : 0.f) : T.bias[job.y];
             float pa = 0.f, pu = 0.f;
 #pragma unroll
             for (int u = 0; u < CH; ++u) {
@@ -647,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                         uu += T.redu[e][w][1];
                     }
                     T.upcnt[e] = 0;
-                    float a = activate(p.act, z + T.bias[job.y]);
+                    float a = activate(p.act, z + bj);
                     if constexpr (GATED) a *= uu;
                     T.a[job.y] = a;
                     __threadfence_block();
@@ -744,6 +860,7 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     p.n_active = a.n_active;
     p.cand = a.cand;
     p.cand_bias = a.cand_bias;
+    p.qent = a.qent;
     p.h = a.h;
     p.status = a.status;
     p.ctrl = a.ctrl;

@@ -26,9 +26,9 @@
 namespace {
 
 // Largest layer this entry point accepts: d_ff <= 65536, rank <= 2048, one
-// token.  ws_layout() of that shape needs 256 + 16 KiB + 8 KiB + 256 KiB +
-// 256 bytes + 256 KiB, rounded up here to 576 KiB.
-constexpr size_t kStaticWsBytes = 576 * 1024;
+// token.  ws_layout() of that shape needs 256 + 16 KiB + 4 KiB + 8 KiB +
+// 256 KiB + 256 bytes + 256 KiB + 512 KiB, rounded up here to 1088 KiB.
+constexpr size_t kStaticWsBytes = 1088 * 1024;
 constexpr int kStaticMaxDff = 65536;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];

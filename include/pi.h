@@ -271,7 +271,7 @@ PI_API pi_status pi_sync_status(void *ws, size_t ws_bytes, pi_stream stream);
  * device-wide synchronisation cudaMalloc / cudaFree can cause).  This entry
  * point is an engineering addition with no counterpart in the method's pages.
  *
- * Scratch space is a fixed file-scope device array of 576 KiB inside the
+ * Scratch space is a fixed file-scope device array of 1088 KiB inside the
  * library, present on every GPU that loads it until the process exits.  Limits:
  * d_ff <= 65536 and rank <= PI_MAX_RANK; larger layers return PI_ERR_SHAPE.
  * The first call on a device looks up the array's device address (once per

@@ -378,3 +378,34 @@ def test_rms_residual_both_paths_and_in_place(d):
     for t in range(3):
         np.testing.assert_allclose(xd[t].cpu().numpy(), oracle.rms_residual(x[t], y[t].astype(np.float64)),
                                    rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("wtype", ["f32", "f16", "q4_0"])
+@pytest.mark.parametrize("gated", [False, True])
+def test_queue_mode_matches_ordered_mode(wtype, gated):
+    """Without idx / n_active, the one-kernel layer takes its FFN rows from a
+    shared work queue instead of an ordered list.  The predicted set is the same
+    (the logits path is deterministic), so its output must match the oracle on
+    the ordered run's resolved list.  Modes alternate on one workspace."""
+    d, F, r = 1024, 4100, 128
+    lay, olay, H = _layer(d, F, r, gated, wtype, seed=131 + gated)
+    X = synth.tokens(4, d, 132).numpy()
+    ws = None
+    for t in range(X.shape[0]):
+        x = _cuda(X[t])
+        idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y1 = torch.empty(d, dtype=torch.float32, device="cuda")
+        ws = B.pi_ffn_layer(lay, x, y1, idx=idx, n_active=n, ws=ws)
+        y2 = torch.empty(d, dtype=torch.float32, device="cuda")
+        B.pi_ffn_layer(lay, x, y2, ws=ws)                       # queue mode
+        B.pi_ffn_layer(lay, x, y2, ws=ws)                       # twice: the counters alternate
+        assert B.pi_sync_status(ws) == 0
+        h, logit_ref, M = oracle.predict(olay, X[t])
+        amb = ambiguous(logit_ref, logit_scale(H, h), olay.threshold)
+        got, ref = set(idx.cpu().numpy()[: int(n.item())].tolist()), set(np.flatnonzero(M).tolist())
+        assert all(amb[j] for j in got ^ ref)
+        res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))), np.int32)
+        y_ref = oracle.sparse_ffn(olay, X[t], res)
+        assert_ffn_close(y1.cpu().numpy(), y_ref, what=f"ordered {wtype} gated={gated} t={t}")
+        assert_ffn_close(y2.cpu().numpy(), y_ref, what=f"queue {wtype} gated={gated} t={t}")
