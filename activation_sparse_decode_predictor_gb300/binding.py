@@ -29,8 +29,8 @@ STATUS_NAMES = {0: "PI_OK", 1: "PI_ERR_NULL", 2: "PI_ERR_SHAPE", 3: "PI_ERR_DTYP
 # every symbol include/pi.h declares
 EXPORTS = ("pi_status_str", "pi_workspace_bytes", "pi_compact_workspace_bytes", "pi_compact", "pi_predict",
            "pi_sparse_ffn", "pi_ffn_layer", "pi_dense_ffn", "pi_q4_0_bytes", "pi_quantize_q4_0",
-           "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_rms_residual", "pi_sync_status",
-           "pi_ffn_layer_static")
+           "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_gather_rows", "pi_shard_neurons",
+           "pi_rms_residual", "pi_sync_status", "pi_ffn_layer_static")
 
 
 class PiError(RuntimeError):
@@ -76,6 +76,8 @@ def lib():
             "pi_fire_counts": ([D, P, i32, P, P], i32),
             "pi_hot_first_perm": ([P, i32, P], i32),
             "pi_permute_rows": ([P, P, i64, i64, P, P], i32),
+            "pi_gather_rows": ([P, i64, P, i64, i64, P, P], i32),
+            "pi_shard_neurons": ([P, i32, i32, i32, P, P], i32),
             "pi_rms_residual": ([P, P, i32, i32, P, P], i32),
             "pi_sync_status": ([P, sz, P], i32),
             "pi_ffn_layer_static": ([D, P, P, P, P, P, P, P], i32),
@@ -155,6 +157,33 @@ class Layer:
         asked into L2 during this layer's FFN phase), or None."""
         self._next = other
         self.desc.next = ctypes.addressof(other.desc) if other is not None else None
+
+    def shard(self, neurons, keep_b_down: bool, stream=None) -> "Layer":
+        """The layer restricted to the neurons listed in `neurons` (device int32,
+        e.g. one shard of pi_shard_neurons): their rows of every per-neuron array
+        gathered in list order, p1 shared.  b_down is kept only when
+        `keep_b_down` (the shard that adds it; the partial outputs of all shards
+        sum to the layer output)."""
+        _dev(neurons, "neurons")
+        n, F, d = int(neurons.numel()), self.d_ff, self.d_model
+        T = self.tensors
+
+        def rows(t):
+            if t is None:
+                return None
+            if self.wtype == PI_Q4_0 and t.dtype == torch.uint8 and t.dim() == 1:
+                codes, scales = F * (d // 2), F * (d // 32) * 2
+                out = torch.empty(q4_0_bytes(n, d), dtype=torch.uint8, device=t.device)
+                pi_gather_rows(t[:codes].view(F, d // 2), neurons, out[: n * (d // 2)].view(n, d // 2), stream)
+                pi_gather_rows(t[codes:codes + scales].view(F, d // 16), neurons,
+                               out[n * (d // 2):].view(n, d // 16), stream)
+                return out
+            return pi_gather_rows(t, neurons, stream=stream)
+
+        return Layer(d, n, self.rank, rows(T["w_up"]), rows(T["w_down"]), w_gate=rows(T["w_gate"]),
+                     b_act=rows(T["b_act"]), b_down=T["b_down"] if keep_b_down else None, p1=T["p1"],
+                     p2=rows(T["p2"]), p_bias=rows(T["p_bias"]), threshold=self.desc.threshold, act=self.desc.act,
+                     wtype=self.wtype)
 
     @classmethod
     def from_dict(cls, L: dict, act=PI_ACT_RELU, threshold=None):
@@ -261,6 +290,28 @@ def pi_permute_rows(src, perm, dst=None, stream=None):
         dst = torch.empty_like(src)
     _check(lib().pi_permute_rows(_p(src), _p(dst), rows, row_bytes, _p(perm), _stream(stream)), "pi_permute_rows")
     return dst
+
+
+def pi_gather_rows(src, idx, dst=None, stream=None):
+    """dst[i] = src[idx[i]] along the first dimension (device tensors)."""
+    rows = src.shape[0]
+    row_bytes = src.numel() * src.element_size() // rows
+    if dst is None:
+        dst = torch.empty((idx.numel(),) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    _check(lib().pi_gather_rows(_p(src), rows, _p(dst), int(dst.shape[0]), row_bytes, _p(idx), _stream(stream)),
+           "pi_gather_rows")
+    return dst
+
+
+def pi_shard_neurons(order, shards: int, shard: int) -> np.ndarray:
+    """Neurons of shard `shard` of `shards` when `order` is dealt round-robin."""
+    o = np.ascontiguousarray(np.asarray(order, dtype=np.int32))
+    out = np.empty(max(1, -(-o.size // max(1, shards))), dtype=np.int32)
+    cnt = np.zeros(1, dtype=np.int32)
+    _check(lib().pi_shard_neurons(o.ctypes.data_as(ctypes.c_void_p), o.size, int(shards), int(shard),
+                                  out.ctypes.data_as(ctypes.c_void_p), cnt.ctypes.data_as(ctypes.c_void_p)),
+           "pi_shard_neurons")
+    return out[: int(cnt[0])].copy()
 
 
 def pi_rms_residual(x, y, out, stream=None):

@@ -11,6 +11,11 @@
 
 namespace pi {
 
+// Row gather of aux.cu (declared here rather than in internal.h, which the
+// fused kernels include).
+cudaError_t launch_gather_rows(const void *src, int64_t src_rows, void *dst, int64_t dst_rows, int64_t row_bytes,
+                               const int *idx, cudaStream_t s);
+
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 WsLayout ws_layout(int d_model, int d_ff, int rank, int batch)
@@ -440,6 +445,33 @@ pi_status pi_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_
     if (!al(perm, 4)) return PI_ERR_ALIGN;
     if (overlap(src, (size_t)(rows * row_bytes), dst, (size_t)(rows * row_bytes))) return PI_ERR_ALIAS;
     return cuda_status(launch_permute_rows(src, dst, rows, row_bytes, perm, (cudaStream_t)stream));
+}
+
+pi_status pi_gather_rows(const void *src, int64_t src_rows, void *dst, int64_t dst_rows, int64_t row_bytes,
+                         const int32_t *idx, pi_stream stream)
+{
+    if (!src || !dst || !idx) return PI_ERR_NULL;
+    if (src_rows < 1 || dst_rows < 1 || row_bytes < 1) return PI_ERR_SHAPE;
+    if (!al(idx, 4)) return PI_ERR_ALIGN;
+    if (overlap(src, (size_t)(src_rows * row_bytes), dst, (size_t)(dst_rows * row_bytes))) return PI_ERR_ALIAS;
+    return cuda_status(launch_gather_rows(src, src_rows, dst, dst_rows, row_bytes, idx, (cudaStream_t)stream));
+}
+
+pi_status pi_shard_neurons(const int32_t *order, int32_t n, int32_t shards, int32_t shard, int32_t *out,
+                           int32_t *count)
+{
+    if (!order || !out || !count) return PI_ERR_NULL;
+    if (n < 1 || shards < 1 || shard < 0 || shard >= shards || shards > n) return PI_ERR_SHAPE;
+    std::vector<uint8_t> seen((size_t)n, 0);
+    for (int32_t p = 0; p < n; ++p) {
+        const int32_t j = order[p];
+        if (j < 0 || j >= n || seen[(size_t)j]) return PI_ERR_INDEX;
+        seen[(size_t)j] = 1;
+    }
+    int32_t c = 0;
+    for (int32_t p = shard; p < n; p += shards) out[c++] = order[p];
+    *count = c;
+    return PI_OK;
 }
 
 pi_status pi_rms_residual(const float *x, const float *y, int32_t batch, int32_t d_model, float *x_next,

@@ -128,27 +128,29 @@ __global__ void __launch_bounds__(256) k_fire_counts(const WT_ *__restrict__ w, 
     }
 }
 
-__global__ void k_permute_rows16(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t rows,
-                                 int64_t vec_per_row, const int *__restrict__ perm)
+// dst row i = src row idx[i] for i < dst_rows; an entry outside [0, src_rows)
+// leaves its destination row unwritten.
+__global__ void k_gather_rows16(const uint4 *__restrict__ src, int64_t src_rows, uint4 *__restrict__ dst,
+                                int64_t dst_rows, int64_t vec_per_row, const int *__restrict__ idx)
 {
-    const int64_t total = rows * vec_per_row;
+    const int64_t total = dst_rows * vec_per_row;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = e / vec_per_row, v = e % vec_per_row;
-        const int pi_ = perm[i];
-        if (pi_ < 0 || pi_ >= rows) continue;
-        dst[e] = src[(int64_t)pi_ * vec_per_row + v];
+        const int r = idx[i];
+        if (r < 0 || r >= src_rows) continue;
+        dst[e] = src[(int64_t)r * vec_per_row + v];
     }
 }
 
-__global__ void k_permute_rows1(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int64_t rows,
-                                int64_t row_bytes, const int *__restrict__ perm)
+__global__ void k_gather_rows1(const uint8_t *__restrict__ src, int64_t src_rows, uint8_t *__restrict__ dst,
+                               int64_t dst_rows, int64_t row_bytes, const int *__restrict__ idx)
 {
-    const int64_t total = rows * row_bytes;
+    const int64_t total = dst_rows * row_bytes;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = e / row_bytes, v = e % row_bytes;
-        const int pi_ = perm[i];
-        if (pi_ < 0 || pi_ >= rows) continue;
-        dst[e] = src[(int64_t)pi_ * row_bytes + v];
+        const int r = idx[i];
+        if (r < 0 || r >= src_rows) continue;
+        dst[e] = src[(int64_t)r * row_bytes + v];
     }
 }
 
@@ -263,20 +265,25 @@ cudaError_t launch_fire_counts(int wtype, const void *w, const float *b, const f
     return cudaGetLastError();
 }
 
-cudaError_t launch_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_bytes, const int *perm,
-                                cudaStream_t s)
+cudaError_t launch_gather_rows(const void *src, int64_t src_rows, void *dst, int64_t dst_rows, int64_t row_bytes,
+                               const int *idx, cudaStream_t s)
 {
     const bool vec = row_bytes % 16 == 0 && ((uintptr_t)src & 15) == 0 && ((uintptr_t)dst & 15) == 0;
     if (vec) {
         const int64_t vpr = row_bytes / 16;
-        k_permute_rows16<<<grid_for(rows * vpr, 256), 256, 0, s>>>(static_cast<const uint4 *>(src),
-                                                                   static_cast<uint4 *>(dst), rows, vpr, perm);
+        k_gather_rows16<<<grid_for(dst_rows * vpr, 256), 256, 0, s>>>(
+            static_cast<const uint4 *>(src), src_rows, static_cast<uint4 *>(dst), dst_rows, vpr, idx);
     } else {
-        k_permute_rows1<<<grid_for(rows * row_bytes, 256), 256, 0, s>>>(static_cast<const uint8_t *>(src),
-                                                                       static_cast<uint8_t *>(dst), rows,
-                                                                       row_bytes, perm);
+        k_gather_rows1<<<grid_for(dst_rows * row_bytes, 256), 256, 0, s>>>(
+            static_cast<const uint8_t *>(src), src_rows, static_cast<uint8_t *>(dst), dst_rows, row_bytes, idx);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_bytes, const int *perm,
+                                cudaStream_t s)
+{
+    return launch_gather_rows(src, rows, dst, rows, row_bytes, perm, s);
 }
 
 cudaError_t launch_rms_residual(const float *x, const float *y, int B, int d, float *out, cudaStream_t s)

@@ -239,14 +239,49 @@ PI_API pi_status pi_fire_counts(const pi_ffn_desc *desc, const float *X, int32_t
 PI_API pi_status pi_hot_first_perm(const int32_t *counts, int32_t n, int32_t *perm);
 
 /*
- * Row gather: dst row i = src row perm[i], for a [rows][row_bytes] byte matrix
- * (device, non-overlapping; perm device int32 [rows] with entries in
- * [0, rows), checked on the device).  Applies a neuron order to w_up / w_gate
- * / w_down / p2 (rows = d_ff) and to the per-neuron vectors b_act / p_bias
- * (row_bytes = 4).  Q4_0 blobs are permuted before quantisation.
+ * Row permutation: dst row i = src row perm[i], for a [rows][row_bytes] byte
+ * matrix (device, non-overlapping; perm device int32 [rows] with entries in
+ * [0, rows); an entry outside that range leaves its destination row
+ * unwritten).  Applies a neuron order to w_up / w_gate / w_down / p2
+ * (rows = d_ff) and to the per-neuron vectors b_act / p_bias (row_bytes = 4).
+ * Q4_0 blobs are permuted before quantisation, or as their two sections (codes
+ * rows of d_model/2 bytes, then scale rows of d_model/16 bytes) separately.
  */
 PI_API pi_status pi_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_bytes,
                           const int32_t *perm, pi_stream stream);
+
+/*
+ * Row gather between matrices of different heights: dst row i = src row idx[i]
+ * for i < dst_rows.  src device [src_rows][row_bytes], dst device
+ * [dst_rows][row_bytes], non-overlapping; idx device int32 [dst_rows], each
+ * entry in [0, src_rows) (an entry outside leaves its destination row
+ * unwritten).  Builds the rows of one neuron shard (pi_shard_neurons) of every
+ * per-neuron array of a layer.  PI_ERR_SHAPE for a non-positive size,
+ * PI_ERR_ALIGN for a misaligned idx, PI_ERR_ALIAS when src and dst overlap.
+ */
+PI_API pi_status pi_gather_rows(const void *src, int64_t src_rows, void *dst, int64_t dst_rows, int64_t row_bytes,
+                         const int32_t *idx, pi_stream stream);
+
+/*
+ * Neuron sharding of one layer over `shards` devices (host, synchronous).
+ * Neurons are independent in the sparse operator -- each one's rows of
+ * w_up / w_gate / w_down, its bias, its predictor row of p2 and p_bias -- so a
+ * layer splits by neuron, as the pages split one FFN between a GPU (hot
+ * neurons) and a CPU (cold neurons) and add the two parts (PowerInfer README
+ * translation, gittoolsai.com, "摘要" abstract and "推理" inference).  p1 is
+ * replicated: every shard computes h itself.  The order (normally the
+ * hot-first order of pi_hot_first_perm, so that every shard gets an equal
+ * share of the frequently active neurons) is dealt round-robin: shard s gets
+ * order[s], order[s + shards], ...
+ * order host int32 [n], a permutation of 0..n-1 (else PI_ERR_INDEX); out host
+ * int32 with room for ceil(n / shards) entries; *count receives the shard's
+ * size.  Each shard runs the layer on its rows and yields a partial y; the
+ * layer output is the sum of the partials (one all-reduce of batch x d_model
+ * fp32 per layer), with b_down and the residual given to one shard only.
+ * PI_ERR_SHAPE unless 1 <= shards <= n and 0 <= shard < shards.
+ */
+PI_API pi_status pi_shard_neurons(const int32_t *order, int32_t n, int32_t shards, int32_t shard, int32_t *out,
+                           int32_t *count);
 
 /*
  * Layer-to-layer glue of a stack of FFN layers whose output feeds the next

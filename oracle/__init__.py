@@ -269,6 +269,31 @@ def rms_residual(x: np.ndarray, y: np.ndarray) -> np.ndarray:
     return out
 
 
+def neuron_shard(L: Layer, neurons: np.ndarray, keep_b_down: bool) -> Layer:
+    """The layer restricted to the listed neurons: row neurons[i] of every
+    per-neuron array (w_up, w_gate, w_down, b_act, p2, p_bias) becomes row i,
+    p1 is shared, b_down is kept only when ``keep_b_down``.  Neurons are
+    independent terms of the FFN sum, so the outputs of shards that partition
+    0..d_ff-1 add up to the layer's output; the pages split one FFN between a
+    GPU (hot neurons) and a CPU (cold neurons) that way (PowerInfer README
+    translation, "摘要" abstract and "推理" inference)."""
+    neurons = np.asarray(neurons, dtype=np.int64)
+    d, F = L.d_model, L.d_ff
+
+    def rows(a):
+        if a is None:
+            return None
+        if L.wtype == Q4_0 and a.ndim == 1 and a.size == q4_0_bytes(F, d):
+            codes = a[: F * (d // 2)].reshape(F, d // 2)[neurons]
+            scales = a[F * (d // 2):].reshape(F, d // 16)[neurons]
+            return np.concatenate([codes.ravel(), scales.ravel()])
+        return np.ascontiguousarray(a[neurons])
+
+    return Layer(d, neurons.size, L.rank, rows(L.w_up), rows(L.w_down), w_gate=rows(L.w_gate),
+                 b_act=rows(L.b_act), b_down=L.b_down if keep_b_down else None, p1=L.p1, p2=rows(L.p2),
+                 p_bias=rows(L.p_bias), threshold=L.threshold, act=L.act)
+
+
 def recall_precision(pred_mask: np.ndarray, true_mask_: np.ndarray):
     """Predictor quality against the true activity: |M&T|/|T| and |M&T|/|M|."""
     m = np.asarray(pred_mask).astype(bool)

@@ -119,6 +119,37 @@ def test_hot_first_perm_errors(L):
     assert L.pi_hot_first_perm(c.ctypes.data_as(ctypes.c_void_p), 0, c.ctypes.data_as(ctypes.c_void_p)) == 2
 
 
+@pytest.mark.parametrize("n,shards", [(1, 1), (10, 3), (11008, 4), (4100, 7)])
+def test_shard_neurons_deal_round_robin(L, n, shards):
+    order = np.random.default_rng(n).permutation(n).astype(np.int32)
+    parts = [B.pi_shard_neurons(order, shards, g) for g in range(shards)]
+    for g, S in enumerate(parts):
+        assert np.array_equal(S, order[g::shards])
+    assert np.array_equal(np.sort(np.concatenate(parts)), np.arange(n))
+    # hot-first order dealt round-robin: every shard's firing total is within
+    # one maximum count of every other's
+    counts = np.random.default_rng(n + 1).integers(0, 50, n).astype(np.int32)
+    hot = B.pi_hot_first_perm(counts)
+    tot = [counts[B.pi_shard_neurons(hot, shards, g)].sum() for g in range(shards)]
+    assert max(tot) - min(tot) <= counts.max()
+
+
+def test_shard_neurons_errors(L):
+    o = np.arange(8, dtype=np.int32)
+    p = o.ctypes.data_as(ctypes.c_void_p)
+    out = np.zeros(8, np.int32)
+    cnt = np.zeros(1, np.int32)
+    po, pc = out.ctypes.data_as(ctypes.c_void_p), cnt.ctypes.data_as(ctypes.c_void_p)
+    assert L.pi_shard_neurons(None, 8, 2, 0, po, pc) == 1
+    assert L.pi_shard_neurons(p, 8, 0, 0, po, pc) == 2
+    assert L.pi_shard_neurons(p, 8, 2, 2, po, pc) == 2
+    assert L.pi_shard_neurons(p, 8, 9, 0, po, pc) == 2
+    bad = np.array([0, 1, 2, 3, 4, 5, 6, 6], np.int32)          # not a permutation
+    assert L.pi_shard_neurons(bad.ctypes.data_as(ctypes.c_void_p), 8, 2, 0, po, pc) == 10
+    bad[7] = 8                                                   # out of range
+    assert L.pi_shard_neurons(bad.ctypes.data_as(ctypes.c_void_p), 8, 2, 0, po, pc) == 10
+
+
 def test_other_entry_validation(L):
     assert L.pi_quantize_q4_0(0x100, 0, 4, 48, 0x200, None) == 2          # cols % 32
     assert L.pi_quantize_q4_0(0x100, 2, 4, 64, 0x200, None) == 3          # source type
@@ -126,5 +157,9 @@ def test_other_entry_validation(L):
     assert L.pi_quantize_q4_0(0x1000, 0, 4, 64, 0x1010, None) == 9       # overlap
     assert L.pi_permute_rows(0x100, 0x1000, 4, 16, None, None) == 1
     assert L.pi_permute_rows(0x100, 0x110, 4, 16, 0x200, None) == 9
+    assert L.pi_gather_rows(0x100, 4, 0x1000, 0, 16, 0x200, None) == 2      # no destination rows
+    assert L.pi_gather_rows(0x100, 4, 0x1000, 2, 16, 0x202, None) == 4      # misaligned idx
+    assert L.pi_gather_rows(0x100, 4, 0x120, 2, 16, 0x200, None) == 9       # dst inside src
+    assert L.pi_gather_rows(None, 4, 0x1000, 2, 16, 0x200, None) == 1
     assert L.pi_rms_residual(0x100, 0x200, 0, 8, 0x300, None) == 2
     assert L.pi_sync_status(None, 0, None) == 8

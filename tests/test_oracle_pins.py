@@ -188,6 +188,36 @@ def test_neuron_permutation_leaves_output_unchanged():
 
 # --- predictor -----------------------------------------------------------------
 
+@pytest.mark.parametrize("shards", [1, 2, 3, 5])
+@pytest.mark.parametrize("gated,wtype,act", [(False, "f16", oracle.ACT_RELU), (True, "q4_0", oracle.ACT_RELU),
+                                             (True, "f32", oracle.ACT_RELU2)])
+def test_neuron_shards_sum_to_the_layer(shards, gated, wtype, act):
+    """Neuron sharding: the shards' partial outputs (b_down on shard 0 only) add
+    up to the layer output computed with float64 matmuls, and each shard's
+    predictor decisions are the layer's decisions on its neurons."""
+    d, F, r = 64, 301, 16
+    lay, w = _np_layer(d, F, r, gated, wtype, seed=41 + shards, act=act)
+    order = np.random.default_rng(shards).permutation(F).astype(np.int32)
+    x = np.random.default_rng(7).standard_normal(d).astype(np.float32)
+    _, _, mask = oracle.predict(lay, x)
+    idx = oracle.compact(mask)
+    y_parts = []
+    for g in range(shards):
+        S = order[g::shards]
+        sh = oracle.neuron_shard(lay, S, keep_b_down=(g == 0))
+        assert sh.d_ff == S.size
+        _, _, m_g = oracle.predict(sh, x)
+        assert np.array_equal(m_g, mask[S])
+        y_parts.append(oracle.sparse_ffn(sh, x, oracle.compact(m_g)))
+    y_ref = oracle.sparse_ffn(lay, x, idx)
+    assert np.allclose(np.sum(y_parts, axis=0), y_ref, rtol=1e-12, atol=1e-12)
+    # the dense layer the same way, against numpy float64 matmuls
+    dense_parts = [oracle.dense_ffn(oracle.neuron_shard(lay, order[g::shards], g == 0), x) for g in range(shards)]
+    assert np.allclose(np.sum(dense_parts, axis=0), _dense_np(lay, w, x)[0], rtol=1e-12, atol=1e-12)
+    if shards > 1:  # dropping a shard is visible
+        assert not np.allclose(np.sum(dense_parts[1:], axis=0), _dense_np(lay, w, x)[0], rtol=1e-6)
+
+
 def test_predictor_matches_float64_formula():
     lay, w = _np_layer(64, 120, 24, False, "f16", seed=41)
     x = synth.tokens(3, 64, 42).numpy()
