@@ -30,6 +30,12 @@
 //      producer (an mbarrier), which asks L2 for all their rows at once and
 //      then runs the FFN jobs as sparse_ffn.cu does; the CTA's partial output
 //      goes to y with 16-byte vector atomics.
+// Steps 2-3 above are the ordered mode, used when the caller asks for the
+// ascending active list.  Without that request (queue mode) there is no
+// barrier B: each CTA appends its range's active neurons to a shared work
+// queue (one 8-byte entry {launch tag, neuron} per neuron) and counts itself
+// done; producers take kQTake queue slots per atomic and stop when the queue
+// is drained and every CTA has published.
 // The grid barriers are counter barriers: one thread per CTA arrives with a
 // release add on a 64-bit counter that is never reset and polls it (acquire,
 // bounded) until it reaches a target derived from a per-launch sequence
@@ -104,11 +110,6 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
