@@ -32,10 +32,11 @@
 //      goes to y with 16-byte vector atomics.
 // Steps 2-3 above are the ordered mode, used when the caller asks for the
 // ascending active list.  Without that request (queue mode) there is no
-// barrier B: each CTA appends its range's active neurons to a shared work
-// queue (one 8-byte entry {launch tag, neuron} per neuron) and counts itself
-// done; producers take kQTake queue slots per atomic and stop when the queue
-// is drained and every CTA has published.
+// barrier B: each CTA keeps the first kOwn active neurons of its own range
+// (its producer starts on them at once, with no global round trip), appends
+// the rest to a shared work queue (one 8-byte entry {launch tag, neuron} per
+// neuron) and counts itself done; producers then take kQTake queue slots per
+// atomic and stop when the queue is drained and every CTA has published.
 // The grid barriers are counter barriers: one thread per CTA arrives with a
 // release add on a 64-bit counter that is never reset and polls it (acquire,
 // bounded) until it reaches a target derived from a per-launch sequence
@@ -62,6 +63,7 @@ constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
 constexpr int kUpRing = 32;        // FFN up rows in flight (> ring stages)
 constexpr int kQTake = 4;          // work-queue slots taken per atomic
+constexpr int kOwn = 4;            // queue mode: active neurons a CTA keeps from its own range
 constexpr int kJobP1 = 1, kJobP2 = 2, kJobUp = 3, kJobDown = 4, kJobEnd = 5;
 
 struct Tables {
@@ -75,7 +77,7 @@ struct Tables {
     unsigned long long seq;
     int share_n;
     int count, total;
-    unsigned qbase;     // queue mode: this CTA's first reserved queue slot
+    unsigned qbase;     // queue mode: the queue slot of the range's k-th active neuron is qbase + k
     int wsum[kNCW];
     unsigned words[kMaxRange / 32 + 1];
     unsigned wpre[kMaxRange / 32 + 1];
@@ -264,11 +266,12 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 }
                 ++q;
             }
-            // FFN jobs: with an ordered active list requested, once the consumers
-            // have found this CTA's share; otherwise (queue mode) from the shared
-            // work queue, once grid barrier A has reset it
+            // FFN jobs, once the consumers have found this CTA's share: with an
+            // ordered active list requested, its slice of that list; otherwise
+            // (queue mode) the first active neurons of its own range, then rows
+            // from the shared work queue
             if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
-            int sn = (failed || qmode) ? 0 : T.share_n;
+            int sn = failed ? 0 : T.share_n;
 #ifndef PI_FUSED_PREFETCH_DOWN
 #define PI_FUSED_PREFETCH_DOWN 0
 #endif
@@ -518,7 +521,6 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     if (t == 0) {
         // every CTA has read this launch's sequence number: move it on
         if (c == 0) atomicAdd(&p.ctrl->bar_seq, 1u);
-        if (qmode) mbar_arrive(&T.share_ready);  // the producer may take queue slots now
     }
     named_bar_sync(1, kNCT);
     for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
@@ -625,16 +627,31 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     }
     named_bar_sync(1, kNCT);
     if (qmode) {
-        // publish this range's active neurons as queue entries, count the CTA as
-        // published (release), and arrive at barrier B without waiting: the FFN
-        // takes its rows from the queue
-        if (t == 0) T.qbase = atomicAdd(&p.ctrl->q_tail[qpar], (unsigned)T.count);
+        // keep the range's first kOwn active neurons and hand them to the
+        // producer; publish the rest as queue entries, count the CTA as
+        // published (release), and arrive at barrier B without waiting
+        const int own = min(T.count, kOwn);
+        for (int wd = warp; wd < nw; wd += kNCW) {
+            const unsigned bits = T.words[wd];
+            if ((bits >> lane) & 1u) {
+                const int k = (int)T.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
+                if (k < own) T.j[k] = j0 + wd * 32 + lane;
+            }
+        }
+        named_bar_sync(1, kNCT);
+        if (t == 0) {
+            T.share_n = ok ? own : 0;
+            mbar_arrive(&T.share_ready);
+            // queue slots for the range's k-th active neuron, k >= own: qbase + k
+            T.qbase = T.count > own ? atomicAdd(&p.ctrl->q_tail[qpar], (unsigned)(T.count - own)) - (unsigned)own : 0u;
+        }
         named_bar_sync(1, kNCT);
         const unsigned tag = (unsigned)T.seq + 1u;
         for (int wd = warp; wd < nw; wd += kNCW) {
             const unsigned bits = T.words[wd];
-            if ((bits >> lane) & 1u) {
-                const int pos = (int)T.qbase + (int)T.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
+            const int k = (int)T.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
+            if (((bits >> lane) & 1u) && k >= own) {
+                const int pos = (int)(T.qbase + (unsigned)k);
                 // tag and neuron in one 8-byte word: a reader that sees the tag sees the neuron
                 const unsigned long long e = ((unsigned long long)tag << 32) | (unsigned)(j0 + wd * 32 + lane);
                 asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.qent + pos), "l"(e) : "memory");
@@ -642,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         named_bar_sync(1, kNCT);
         if (t == 0) {
-            __threadfence();
+            // the release covers the q_tail reservation above; each entry carries
+            // its own launch tag, so readers need no ordering for the entries
             asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.ctrl->q_done[qpar]) : "memory");
             asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&p.ctrl->bar_ctr) : "memory");
         }

@@ -380,15 +380,19 @@ def test_rms_residual_both_paths_and_in_place(d):
                                    rtol=1e-5, atol=1e-6)
 
 
-@pytest.mark.parametrize("wtype", ["f32", "f16", "q4_0"])
-@pytest.mark.parametrize("gated", [False, True])
-def test_queue_mode_matches_ordered_mode(wtype, gated):
-    """Without idx / n_active, the one-kernel layer takes its FFN rows from a
-    shared work queue instead of an ordered list.  The predicted set is the same
-    (the logits path is deterministic), so its output must match the oracle on
-    the ordered run's resolved list.  Modes alternate on one workspace."""
+@pytest.mark.parametrize("wtype,gated,sparsity", [("f32", False, 0.8), ("f32", True, 0.8), ("f16", False, 0.8),
+                                                  ("f16", True, 0.8), ("q4_0", False, 0.8), ("q4_0", True, 0.8),
+                                                  ("f16", True, 0.4), ("f16", False, 0.995)])
+def test_queue_mode_matches_ordered_mode(wtype, gated, sparsity):
+    """Without idx / n_active, the one-kernel layer keeps the first active
+    neurons of each CTA's range and takes the rest from a shared work queue
+    instead of an ordered list.  The predicted set is the same (the logits path
+    is deterministic), so its output must match the oracle on the ordered run's
+    resolved list.  Densities span ranges with fewer active neurons than a CTA
+    keeps (a nearly empty queue) and far more.  Modes alternate on one
+    workspace."""
     d, F, r = 1024, 4100, 128
-    lay, olay, H = _layer(d, F, r, gated, wtype, seed=131 + gated)
+    lay, olay, H = _layer(d, F, r, gated, wtype, seed=131 + gated, sparsity=sparsity)
     X = synth.tokens(4, d, 132).numpy()
     ws = None
     for t in range(X.shape[0]):
