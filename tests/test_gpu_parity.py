@@ -380,6 +380,34 @@ def test_rms_residual_both_paths_and_in_place(d):
                                    rtol=1e-5, atol=1e-6)
 
 
+@pytest.mark.parametrize("ptype,rank", [("f16", 2048), ("f32", 768)])
+def test_wide_rank_layer(ptype, rank):
+    """Predictor ranks wider than the per-lane register slices of h (fp16 above
+    1024, fp32 above 512): the one-kernel layer reads the rest of h from
+    shared memory.  Ordered and queue mode against the oracle."""
+    d, F = 1024, 4100
+    lay, olay, H = _layer(d, F, rank, True, ptype, seed=171 + rank, sparsity=0.85)
+    X = synth.tokens(2, d, 172).numpy()
+    ws = None
+    for t in range(X.shape[0]):
+        x = _cuda(X[t])
+        idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y1 = torch.empty(d, dtype=torch.float32, device="cuda")
+        ws = B.pi_ffn_layer(lay, x, y1, idx=idx, n_active=n, ws=ws)
+        y2 = torch.empty(d, dtype=torch.float32, device="cuda")
+        B.pi_ffn_layer(lay, x, y2, ws=ws)
+        assert B.pi_sync_status(ws) == 0
+        h, logit_ref, M = oracle.predict(olay, X[t])
+        amb = ambiguous(logit_ref, logit_scale(H, h), olay.threshold)
+        got, ref = set(idx.cpu().numpy()[: int(n.item())].tolist()), set(np.flatnonzero(M).tolist())
+        assert all(amb[j] for j in got ^ ref)
+        res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))), np.int32)
+        y_ref = oracle.sparse_ffn(olay, X[t], res)
+        assert_ffn_close(y1.cpu().numpy(), y_ref, what=f"ordered {ptype} r={rank} t={t}")
+        assert_ffn_close(y2.cpu().numpy(), y_ref, what=f"queue {ptype} r={rank} t={t}")
+
+
 @pytest.mark.parametrize("wtype,gated,sparsity", [("f32", False, 0.8), ("f32", True, 0.8), ("f16", False, 0.8),
                                                   ("f16", True, 0.8), ("q4_0", False, 0.8), ("q4_0", True, 0.8),
                                                   ("f16", True, 0.4), ("f16", False, 0.995)])
