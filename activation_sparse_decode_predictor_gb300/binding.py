@@ -171,7 +171,8 @@ class Layer:
         def rows(t):
             if t is None:
                 return None
-            if self.wtype == PI_Q4_0 and t.dtype == torch.uint8 and t.dim() == 1:
+            if self.wtype == PI_Q4_0 and t.dtype == torch.uint8:
+                t = t.reshape(-1)  # the blob: all code rows, then all scale rows
                 codes, scales = F * (d // 2), F * (d // 32) * 2
                 out = torch.empty(q4_0_bytes(n, d), dtype=torch.uint8, device=t.device)
                 pi_gather_rows(t[:codes].view(F, d // 2), neurons, out[: n * (d // 2)].view(n, d // 2), stream)
