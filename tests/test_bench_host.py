@@ -1,0 +1,52 @@
+"""Host-side arithmetic of bench.py, on CPU: the algorithmic (needed) bytes that
+the roofline divides by, checked against the expected per-token figures worked
+out by hand from the configured shapes and densities, and the statistics-only
+Q4_0 dequantiser checked against the oracle's."""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_sparse_decode_predictor_gb300 import synth
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+# expected active rows at the configured density (n = (1 - sparsity) * d_ff,
+# down rows = n) and the resulting needed megabytes per token and layer:
+#   predictor (r*d + F*r) * 2 B, n * (R*g + 4) + n * R, x in and y out
+@pytest.mark.parametrize("name,n,mb", [
+    ("llama7b-reglu-fp16", 1101, 58.0),      # 30.9 predictor + 27.1 FFN
+    ("opt30b-relu-fp16-perm", 1434, 114.6),
+    ("falcon40b-relu-fp16", 3277, 191.2),
+    ("falcon40b-relu-q4_0", 3277, 114.2),
+    ("opt175b-relu-fp16-stack12", 2458, 246.7),
+])
+def test_needed_bytes_at_configured_density(name, n, mb):
+    w = synth.WORKLOADS[name]
+    pred, ffn = bench.needed_bytes(w, n, n)
+    assert (pred + ffn) / 1e6 == pytest.approx(mb, abs=0.15)
+    # the predictor term alone: both matrices once, at the predictor element size
+    assert pred == (w.rank * w.d_model + w.d_ff * w.rank) * 2
+
+
+def test_needed_bytes_terms():
+    w = synth.WORKLOADS["llama7b-reglu-fp16"]
+    # one more predicted neuron adds its gate and up rows plus a 4-byte index;
+    # one more non-zero neuron adds its down row; a group of B tokens adds B x/y
+    p0, f0 = bench.needed_bytes(w, 100, 50)
+    assert bench.needed_bytes(w, 101, 50)[1] - f0 == 2 * 2 * w.d_model + 4
+    assert bench.needed_bytes(w, 100, 51)[1] - f0 == 2 * w.d_model
+    p4, f4 = bench.needed_bytes(w, 100, 50, batch=4)
+    assert p4 == p0 and f4 - f0 == 3 * 2 * 4 * w.d_model
+
+
+def test_q4_dequant_helper_matches_oracle():
+    rows, cols = 7, 96
+    blob = oracle.q4_0_quantize(np.random.default_rng(3).standard_normal((rows, cols)).astype(np.float32))
+    got = bench.q4_dequant_torch(torch.from_numpy(blob), rows, cols).numpy().astype(np.float64)
+    assert np.array_equal(got, oracle.dequantize(blob, rows, cols))
