@@ -327,6 +327,15 @@ def oracle_stack_sample(w, olays, X_host, budget_s):
     return (time.perf_counter() - t0) / (done * len(olays)) * 1e6, done
 
 
+def oracle_dense_us(olay, x):
+    """Context for the reference arm: the oracle's dense FFN (every neuron) on
+    one token, microseconds."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.dense_ffn(olay, x)
+    return (time.perf_counter() - t0) * 1e6
+
+
 def oracle_layer(w, H):
     import oracle
     return oracle.Layer(w.d_model, w.d_ff, w.rank, H["w_up"], H["w_down"], w_gate=H["w_gate"], b_act=H["b_act"],
@@ -360,7 +369,9 @@ def run_reference(args, w):
                 "cpu_baseline": {"value": value, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
                                  "sample": f"{ntok} token(s) per step through all {w.layers} layers, "
                                            "single-threaded C, fp64"},
-                "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "cpu_dense": {"value": oracle_dense_us(olays[0], X[0]), "unit": "us/layer/token",
+                              "sample": "1 token through layer 0, every neuron, single-threaded C oracle, fp64"}}
         print(json.dumps(line))
         return 0
     L0 = synth.workload_layer(w, 0, device="cpu")
@@ -384,7 +395,9 @@ def run_reference(args, w):
             "cpu_baseline": {"value": value, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
                              "sample": f"{tokens_per_sample} token(s) per step through one layer (predictor, "
                                        "compaction, sparse FFN), single-threaded C, fp64"},
-            "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "cpu_dense": {"value": oracle_dense_us(oracle_layer(w, H), X[0]), "unit": "us/layer/token",
+                          "sample": "1 token, every neuron, single-threaded C oracle, fp64"}}
     print(json.dumps(line))
     return 0
 

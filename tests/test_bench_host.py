@@ -50,3 +50,23 @@ def test_q4_dequant_helper_matches_oracle():
     blob = oracle.q4_0_quantize(np.random.default_rng(3).standard_normal((rows, cols)).astype(np.float32))
     got = bench.q4_dequant_torch(torch.from_numpy(blob), rows, cols).numpy().astype(np.float64)
     assert np.array_equal(got, oracle.dequantize(blob, rows, cols))
+
+
+@pytest.mark.parametrize("layers", [1, 3])
+def test_reference_arm_prints_one_contract_line(layers, capsys, monkeypatch):
+    """The reference arm (the oracle on the host cores) on a small workload:
+    one JSON line with the contract's keys, in one or several layers."""
+    import argparse
+    import json
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    w = synth.Workload("small-stack", 256, 1024, 32, False, "f16", 0.9, 8, layers=layers, predictor="random",
+                       seed=7)
+    args = argparse.Namespace(gpus=1, steps=2, warmup=3, cpu_seconds=1.0, one_layer=False)
+    assert bench.run_reference(args, w) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "us/layer/token" and line["higher_is_better"] is False
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "us/layer/token", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["cpu_dense"]["value"] > 0
+    assert line["config"]["workload"] == "small-stack"
