@@ -29,7 +29,7 @@ def _rank(rank, world, port, local_ms, out):
 def test_two_ranks_take_the_slowest_time():
     world, local_ms = 2, [4.0, 6.5]
     port = 29500 + (os.getpid() % 1000)
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(world, port, local_ms, out), nprocs=world, start_method="spawn")
         res = dict(out)

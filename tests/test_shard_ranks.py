@@ -64,7 +64,7 @@ def test_two_rank_sharded_layer_equals_the_layer():
     build.build()
     world = 2
     port = 29700 + (os.getpid() % 1000)
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
