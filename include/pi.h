@@ -197,6 +197,13 @@ PI_API pi_status pi_sparse_ffn(const pi_ffn_desc *desc, const float *x, int32_t 
  *   idx / n_active  device int32 [d_ff] / [1] receiving the active list, or
  *                   NULL to keep it inside the workspace.
  *   other arguments as in pi_sparse_ffn.
+ * At batch 1 (for the shapes it supports) the whole step is one kernel of one
+ * CTA per SM whose CTAs synchronise across the grid, so it needs all of them
+ * resident at once.  If other streams or processes hold SMs long enough, its
+ * bounded waits give up: PI_ERR_TIMEOUT from pi_sync_status, and y is not
+ * valid.  With idx / n_active NULL the FFN rows are spread over the CTAs
+ * dynamically; otherwise the ascending list is also written, which costs one
+ * more grid-wide synchronisation.
  */
 PI_API pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual,
                        float *y, int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes,
