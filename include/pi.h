@@ -62,7 +62,8 @@ typedef enum {
     PI_ERR_TIMEOUT = 7,   /* device: a bounded wait gave up                          */
     PI_ERR_WORKSPACE = 8, /* workspace missing or smaller than required              */
     PI_ERR_ALIAS = 9,     /* an output overlaps an input it may not overlap          */
-    PI_ERR_INDEX = 10     /* device: a neuron index was outside [0, d_ff)            */
+    PI_ERR_INDEX = 10     /* a neuron index out of range (device), or a host neuron
+                             order that is not a permutation (pi_shard_neurons)     */
 } pi_status;
 
 typedef enum { PI_F32 = 0, PI_F16 = 1, PI_Q4_0 = 2 } pi_dtype;
