@@ -293,6 +293,25 @@ def test_q4_0_layout_and_error_bound():
             assert np.all(err <= bound)
 
 
+def test_q4_0_hand_worked_block():
+    """A block quantised by hand (tests/golden/hand_worked_q4_0.txt): scale
+    choice, half-up rounding, the clamp at 15, nibble order and the split
+    layout, byte for byte."""
+    fields = {}
+    for line in open(os.path.join(GOLDEN, "hand_worked_q4_0.txt")):
+        line = line.split("#", 1)[0].strip()
+        if "=" in line:
+            k, v = line.split("=", 1)
+            fields[k.strip()] = v.split()
+    w = np.zeros((1, 32), dtype=np.float32)
+    for item in fields["w"]:
+        e, v = item.split(":")
+        w[0, int(e)] = np.float32(float(v))
+    blob = oracle.q4_0_quantize(w)
+    assert blob.tobytes() == bytes(int(b, 16) for b in fields["bytes"])
+    assert np.array_equal(oracle.dequantize(blob, 1, 32)[0], np.array([float(v) for v in fields["dequant"]]))
+
+
 def test_q4_0_zero_block():
     blob = oracle.q4_0_quantize(np.zeros((2, 32), np.float32))
     assert np.all(blob[:32] == 0x88) and np.all(blob[32:] == 0)
