@@ -359,6 +359,26 @@ def _read_golden(name):
     return vals
 
 
+@pytest.mark.parametrize("act,tag", [(oracle.ACT_RELU, "reglu"), (oracle.ACT_RELU2, "relu2")])
+def test_hand_worked_gated_example(act, tag):
+    g = _read_golden("hand_worked_reglu.txt")
+    d, F, r = 2, 3, 2
+    f32 = lambda k, shape: g[k].reshape(shape).astype(np.float32)
+    lay = oracle.Layer(d, F, r, f32("w_up", (F, d)), f32("w_down", (F, d)), w_gate=f32("w_gate", (F, d)),
+                       b_act=g["b_act"], b_down=g["b_down"], p1=f32("p1", (r, d)), p2=f32("p2", (F, r)),
+                       p_bias=g["p_bias"], threshold=float(g["threshold"][0]), act=act)
+    x = g["x"].astype(np.float32)
+    h, logit, mask = oracle.predict(lay, x)
+    assert np.array_equal(h, g["h"]) and np.array_equal(logit, g["logit"])
+    idx = oracle.compact(mask)
+    assert np.array_equal(idx, g["idx"].astype(np.int32))
+    T, _ = oracle.true_mask(lay, x)
+    assert np.array_equal(T, np.array([1, 1, 0], dtype=np.uint8))
+    assert oracle.recall_precision(mask, T) == (g["recall"][0], g["precision"][0])
+    assert np.array_equal(oracle.dense_ffn(lay, x), g["y_dense_" + tag])
+    assert np.array_equal(oracle.sparse_ffn(lay, x, idx), g["y_sparse_" + tag])
+
+
 def test_hand_worked_example():
     g = _read_golden("hand_worked_ffn.txt")
     d, F, r = 3, 4, 2
