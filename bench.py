@@ -68,15 +68,21 @@ def parse():
 
 # ------------------------------------------------------------------------------------ helpers
 def measured_peaks():
+    """HBM copy bandwidth (GB/s) from MEASURED_PEAKS.json when present: a
+    number under hbm_gbs (or hbm_GBps / hbm), or an object holding one under
+    value / burst / median / mean; else the fallback figure."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
             with open(p) as f:
                 d = json.load(f)
             for k in ("hbm_gbs", "hbm_GBps", "hbm"):
-                if k in d:
-                    return float(d[k]), "measured"
-        except Exception:  # noqa: BLE001
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = next((v[q] for q in ("value", "burst", "median", "mean") if q in v), None)
+                if isinstance(v, (int, float)) and v > 0:
+                    return float(v), "measured"
+        except Exception:  # noqa: BLE001 -- an unreadable file means the fallback
             pass
     return FALLBACK_HBM_GBS, "fallback"
 

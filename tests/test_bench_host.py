@@ -70,3 +70,22 @@ def test_reference_arm_prints_one_contract_line(layers, capsys, monkeypatch):
                            "d2h_bytes_per_step": 0}
     assert line["cpu_dense"]["value"] > 0
     assert line["config"]["workload"] == "small-stack"
+
+
+@pytest.mark.parametrize("content,want", [
+    (None, None),
+    ('{"hbm_gbs": 7012.5, "bf16_tflops": 2100}', 7012.5),
+    ('{"hbm_gbs": {"value": 6900, "unit": "GB/s"}}', 6900.0),
+    ('{"hbm": {"burst": 7100.0}}', 7100.0),
+    ('{"bf16_tflops": 2100}', None),
+    ('not json', None),
+])
+def test_measured_peaks_file(tmp_path, monkeypatch, content, want):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    if content is not None:
+        (tmp_path / "MEASURED_PEAKS.json").write_text(content)
+    peak, src = bench.measured_peaks()
+    if want is None:
+        assert (peak, src) == (bench.FALLBACK_HBM_GBS, "fallback")
+    else:
+        assert (peak, src) == (want, "measured")
