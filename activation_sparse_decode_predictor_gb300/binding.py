@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "PI_OK", 1: "PI_ERR_NULL", 2: "PI_ERR_SHAPE", 3: "PI_ERR_DTYP
 # every symbol include/pi.h declares
 EXPORTS = ("pi_status_str", "pi_workspace_bytes", "pi_compact_workspace_bytes", "pi_compact", "pi_predict",
            "pi_sparse_ffn", "pi_ffn_layer", "pi_dense_ffn", "pi_q4_0_bytes", "pi_quantize_q4_0",
-           "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_gather_rows", "pi_shard_neurons",
+           "pi_quantize_q4_0_host", "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_gather_rows",
+           "pi_shard_neurons",
            "pi_rms_residual", "pi_sync_status", "pi_ffn_layer_static")
 
 
@@ -73,6 +74,7 @@ def lib():
             "pi_dense_ffn": ([D, P, i32, P, P, P, sz, P], i32),
             "pi_q4_0_bytes": ([i64, i64], sz),
             "pi_quantize_q4_0": ([P, i32, i64, i64, P, P], i32),
+            "pi_quantize_q4_0_host": ([P, i64, i64, P], i32),
             "pi_fire_counts": ([D, P, i32, P, P], i32),
             "pi_hot_first_perm": ([P, i32, P], i32),
             "pi_permute_rows": ([P, P, i64, i64, P, P], i32),
@@ -269,6 +271,16 @@ def pi_quantize_q4_0(src, dst=None, stream=None):
         dst = torch.empty(q4_0_bytes(rows, cols), dtype=torch.uint8, device=src.device)
     _check(lib().pi_quantize_q4_0(_p(src), st, rows, cols, _p(dst), _stream(stream)), "pi_quantize_q4_0")
     return dst
+
+
+def pi_quantize_q4_0_host(w) -> np.ndarray:
+    """Q4_0 blob of a host fp32 [rows, cols] matrix, quantised on the CPU by the library."""
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float32))
+    rows, cols = w.shape
+    out = np.empty(max(1, q4_0_bytes(rows, cols)), dtype=np.uint8)
+    _check(lib().pi_quantize_q4_0_host(w.ctypes.data_as(ctypes.c_void_p), rows, cols,
+                                       out.ctypes.data_as(ctypes.c_void_p)), "pi_quantize_q4_0_host")
+    return out
 
 
 def pi_fire_counts(layer: Layer, X, counts, stream=None):

@@ -2,6 +2,8 @@
 // workspace layout and kernel sequencing.  Declarations and the contract of
 // each call are in include/pi.h.
 #include <algorithm>
+#include <cmath>
+#include <cstring>
 #include <mutex>
 #include <numeric>
 #include <vector>
@@ -411,6 +413,74 @@ pi_status pi_quantize_q4_0(const void *src, int32_t src_type, int64_t rows, int6
     const size_t nsrc = (size_t)rows * cols * (src_type == PI_F32 ? 4 : 2);
     if (overlap(src, nsrc, dst, pi_q4_0_bytes(rows, cols))) return PI_ERR_ALIAS;
     return cuda_status(launch_quantize_q4_0(src, src_type, rows, cols, dst, (cudaStream_t)stream));
+}
+
+// binary32 -> binary16, round to nearest, ties to even (IEEE 754 conversion,
+// written from the format definitions): normal results by integer rounding of
+// the 23-bit significand to 10 bits, subnormal results by rounding |f| * 2^24
+// to an integer (exact scaling, then the FP environment's ties-to-even).
+static uint16_t host_f32_to_f16(float f)
+{
+    uint32_t x;
+    std::memcpy(&x, &f, 4);
+    const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    const uint32_t ax = x & 0x7fffffffu;
+    if (ax > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);  // NaN
+    if (ax >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u);  // >= 65520 rounds to infinity
+    if (ax < 0x38800000u) {                                     // below 2^-14: subnormal or zero
+        const float m = std::nearbyint(std::fabs(f) * 16777216.0f);  // |f| * 2^24, exact
+        return (uint16_t)(sign | (uint16_t)m);                  // m == 1024 is the smallest normal
+    }
+    const uint32_t e = (ax >> 23) - 127 + 15, mant = ax & 0x7fffffu;
+    uint32_t h = (e << 10) | (mant >> 13);
+    const uint32_t rest = mant & 0x1fffu;
+    if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) ++h;   // carries into the exponent as it should
+    return (uint16_t)(sign | h);
+}
+
+static float host_f16_to_f32(uint16_t h)
+{
+    const uint32_t e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+    float v;
+    if (e == 0) v = std::ldexp((float)m, -24);
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = std::ldexp((float)(m | 0x400u), (int)e - 25);
+    return (h & 0x8000u) ? -v : v;
+}
+
+pi_status pi_quantize_q4_0_host(const float *src, int64_t rows, int64_t cols, void *dst)
+{
+    if (!src || !dst) return PI_ERR_NULL;
+    if (rows < 1 || cols < 32 || cols % 32) return PI_ERR_SHAPE;
+    if (overlap(src, (size_t)rows * cols * 4, dst, pi_q4_0_bytes(rows, cols))) return PI_ERR_ALIAS;
+    uint8_t *codes = static_cast<uint8_t *>(dst);
+    uint8_t *scales = codes + (size_t)rows * (size_t)(cols / 2);
+    const int64_t nb = cols / 32;
+    for (int64_t j = 0; j < rows; ++j) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *w = src + j * cols + b * 32;
+            float amax = w[0];  // the first weight of largest magnitude
+            for (int e = 1; e < 32; ++e)
+                if (std::fabs(w[e]) > std::fabs(amax)) amax = w[e];
+            const float s32 = amax / -8.0f;
+            const uint16_t s16 = s32 == 0.0f ? (uint16_t)0 : host_f32_to_f16(s32);
+            const float sc = host_f16_to_f32(s16);
+            uint8_t q[32];
+            for (int e = 0; e < 32; ++e) {
+                int qi = 8;
+                if (sc != 0.0f) {
+                    volatile float t = w[e] / sc;  // binary32 quotient, then binary32 sum
+                    const float fl = std::floor(t + 8.5f);
+                    qi = fl < 0.0f ? 0 : (fl > 15.0f ? 15 : (int)fl);
+                }
+                q[e] = (uint8_t)qi;
+            }
+            uint8_t *cb = codes + j * (cols / 2) + b * 16;
+            for (int e = 0; e < 16; ++e) cb[e] = (uint8_t)(q[e] | (q[e + 16] << 4));
+            std::memcpy(scales + 2 * (size_t)(j * nb + b), &s16, 2);  // little-endian binary16
+        }
+    }
+    return PI_OK;
 }
 
 pi_status pi_fire_counts(const pi_ffn_desc *desc, const float *X, int32_t T, int32_t *counts, pi_stream stream)

@@ -230,6 +230,16 @@ PI_API pi_status pi_quantize_q4_0(const void *src, int32_t src_type, int64_t row
                            pi_stream stream);
 
 /*
+ * The same quantiser on the host (synchronous, needs no GPU), for offline
+ * conversion of checkpoints: byte for byte what pi_quantize_q4_0 writes for
+ * fp32 input.
+ *   src  host fp32 [rows][cols], row-major; cols % 32 == 0 (else PI_ERR_SHAPE).
+ *   dst  host buffer of pi_q4_0_bytes(rows, cols) bytes, not overlapping src
+ *        (else PI_ERR_ALIAS).
+ */
+PI_API pi_status pi_quantize_q4_0_host(const float *src, int64_t rows, int64_t cols, void *dst);
+
+/*
  * Offline activation profiling (PowerInfer summary, "方法详解": hot neurons
  * are found by analysing the activation distribution offline): for each of
  * the T tokens of X (device fp32 [T][d_model]), counts[j] += 1 when the

@@ -150,11 +150,47 @@ def test_shard_neurons_errors(L):
     assert L.pi_shard_neurons(bad.ctypes.data_as(ctypes.c_void_p), 8, 2, 0, po, pc) == 10
 
 
+@pytest.mark.parametrize("scale", [1.0, 1e-3, 3e-6, 1e-7, 250.0])
+def test_host_quantiser_matches_oracle(L, scale):
+    """pi_quantize_q4_0_host against the oracle's quantiser, byte for byte, at
+    magnitudes whose scales are normal, subnormal and flushed to zero in
+    binary16, with zero blocks and exact rounding ties mixed in."""
+    rng = np.random.default_rng(int(scale * 1e7) % 1000 + 5)
+    rows, cols = 37, 256
+    w = (rng.standard_normal((rows, cols)) * scale).astype(np.float32)
+    w[3, 32:64] = 0.0                                       # a zero block
+    w[5, :32] = np.float32(scale) * np.arange(-16, 16, dtype=np.float32) / 2   # steps and half steps
+    w[6, 64:96] = -w[6, 64:96]
+    got = B.pi_quantize_q4_0_host(w)
+    assert np.array_equal(got, oracle.q4_0_quantize(w))
+
+
+def test_host_quantiser_across_binary16_range(L):
+    """Blocks whose scales sweep binary16 from below its smallest subnormal to
+    near its largest normal, through the subnormal/normal boundary."""
+    rng = np.random.default_rng(11)
+    rows = 400
+    mags = np.logspace(-9, 5.5, rows).astype(np.float32)
+    w = (rng.standard_normal((rows, 64)) * mags[:, None]).astype(np.float32)
+    assert np.array_equal(B.pi_quantize_q4_0_host(w), oracle.q4_0_quantize(w))
+
+
+def test_host_quantiser_hand_worked_block(L):
+    w = np.zeros((1, 32), np.float32)
+    for e, v in {0: 1.0, 1: -4.0, 2: 3.5, 3: 0.3, 4: 0.25, 5: -0.25, 6: 4.0, 7: -3.9, 16: 2.0, 17: -1.75,
+                 31: 0.74}.items():
+        w[0, e] = v
+    assert B.pi_quantize_q4_0_host(w).tobytes() == bytes.fromhex("CA508F8989888F8088888888888888980038")
+
+
 def test_other_entry_validation(L):
     assert L.pi_quantize_q4_0(0x100, 0, 4, 48, 0x200, None) == 2          # cols % 32
     assert L.pi_quantize_q4_0(0x100, 2, 4, 64, 0x200, None) == 3          # source type
     assert L.pi_quantize_q4_0(0x100, 0, 4, 64, 0x108, None) == 4
     assert L.pi_quantize_q4_0(0x1000, 0, 4, 64, 0x1010, None) == 9       # overlap
+    assert L.pi_quantize_q4_0_host(None, 4, 64, 0x100) == 1
+    assert L.pi_quantize_q4_0_host(0x100, 4, 48, 0x100000) == 2           # cols % 32
+    assert L.pi_quantize_q4_0_host(0x1000, 4, 64, 0x1010) == 9           # overlap
     assert L.pi_permute_rows(0x100, 0x1000, 4, 16, None, None) == 1
     assert L.pi_permute_rows(0x100, 0x110, 4, 16, 0x200, None) == 9
     assert L.pi_gather_rows(0x100, 4, 0x1000, 0, 16, 0x200, None) == 2      # no destination rows
