@@ -8,6 +8,8 @@
 #include <numeric>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 #include "pi.h"
 
@@ -85,6 +87,14 @@ using namespace pi;
 namespace {
 
 inline bool al(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// A named NVTX range around the host side of an entry point (the enqueue), so
+// profilers can attribute the kernels each call launches; costs a pointer
+// check when no tool is attached.
+struct Nvtx {
+    explicit Nvtx(const char *name) { nvtxRangePushA(name); }
+    ~Nvtx() { nvtxRangePop(); }
+};
 
 inline bool overlap(const void *a, size_t an, const void *b, size_t bn)
 {
@@ -271,6 +281,7 @@ size_t pi_compact_workspace_bytes(int32_t n) { return n < 1 ? 0 : compact_ws_byt
 pi_status pi_compact(const uint8_t *mask, int32_t n, int32_t *idx, int32_t *count, int32_t cap, void *ws,
                      size_t ws_bytes, pi_stream stream)
 {
+    Nvtx nv("pi_compact");
     if (!mask || !idx || !count) return PI_ERR_NULL;
     if (n < 1 || cap < 1) return PI_ERR_SHAPE;
     if (!al(idx, 4) || !al(count, 4)) return PI_ERR_ALIGN;
@@ -283,6 +294,7 @@ pi_status pi_compact(const uint8_t *mask, int32_t n, int32_t *idx, int32_t *coun
 pi_status pi_predict(const pi_ffn_desc *desc, const float *x, int32_t batch, float *logits, uint8_t *mask,
                      int32_t *idx, int32_t *n_active, int32_t cap, void *ws, size_t ws_bytes, pi_stream stream)
 {
+    Nvtx nv("pi_predict");
     pi_status st = check_desc(desc, false, true);
     if (st != PI_OK) return st;
     if (batch < 1 || batch > PI_MAX_BATCH || cap < 1) return PI_ERR_SHAPE;
@@ -298,6 +310,7 @@ pi_status pi_sparse_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, 
                         const int32_t *n_active, const float *residual, float *y, void *ws, size_t ws_bytes,
                         pi_stream stream)
 {
+    Nvtx nv("pi_sparse_ffn");
     pi_status st = check_desc(desc, true, false);
     if (st != PI_OK) return st;
     st = check_io(desc, x, batch, residual, y);
@@ -315,6 +328,7 @@ pi_status pi_sparse_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, 
 pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,
                        int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes, pi_stream stream)
 {
+    Nvtx nv("pi_ffn_layer");
     pi_status st = check_desc(desc, true, true);
     if (st != PI_OK) return st;
     st = check_io(desc, x, batch, residual, y);
@@ -382,6 +396,7 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
 pi_status pi_dense_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,
                        void *ws, size_t ws_bytes, pi_stream stream)
 {
+    Nvtx nv("pi_dense_ffn");
     pi_status st = check_desc(desc, true, false);
     if (st != PI_OK) return st;
     st = check_io(desc, x, batch, residual, y);
@@ -406,6 +421,7 @@ size_t pi_q4_0_bytes(int64_t rows, int64_t cols)
 pi_status pi_quantize_q4_0(const void *src, int32_t src_type, int64_t rows, int64_t cols, void *dst,
                            pi_stream stream)
 {
+    Nvtx nv("pi_quantize_q4_0");
     if (!src || !dst) return PI_ERR_NULL;
     if (src_type != PI_F32 && src_type != PI_F16) return PI_ERR_DTYPE;
     if (rows < 1 || cols < 32 || cols % 32) return PI_ERR_SHAPE;
@@ -450,6 +466,7 @@ static float host_f16_to_f32(uint16_t h)
 
 pi_status pi_quantize_q4_0_host(const float *src, int64_t rows, int64_t cols, void *dst)
 {
+    Nvtx nv("pi_quantize_q4_0_host");
     if (!src || !dst) return PI_ERR_NULL;
     if (rows < 1 || cols < 32 || cols % 32) return PI_ERR_SHAPE;
     if (overlap(src, (size_t)rows * cols * 4, dst, pi_q4_0_bytes(rows, cols))) return PI_ERR_ALIAS;
@@ -485,6 +502,7 @@ pi_status pi_quantize_q4_0_host(const float *src, int64_t rows, int64_t cols, vo
 
 pi_status pi_fire_counts(const pi_ffn_desc *desc, const float *X, int32_t T, int32_t *counts, pi_stream stream)
 {
+    Nvtx nv("pi_fire_counts");
     pi_status st = check_desc(desc, true, false);
     if (st != PI_OK) return st;
     if (desc->wtype == PI_Q4_0) return PI_ERR_DTYPE;
@@ -510,6 +528,7 @@ pi_status pi_hot_first_perm(const int32_t *counts, int32_t n, int32_t *perm)
 pi_status pi_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_bytes, const int32_t *perm,
                           pi_stream stream)
 {
+    Nvtx nv("pi_permute_rows");
     if (!src || !dst || !perm) return PI_ERR_NULL;
     if (rows < 1 || row_bytes < 1) return PI_ERR_SHAPE;
     if (!al(perm, 4)) return PI_ERR_ALIGN;
@@ -520,6 +539,7 @@ pi_status pi_permute_rows(const void *src, void *dst, int64_t rows, int64_t row_
 pi_status pi_gather_rows(const void *src, int64_t src_rows, void *dst, int64_t dst_rows, int64_t row_bytes,
                          const int32_t *idx, pi_stream stream)
 {
+    Nvtx nv("pi_gather_rows");
     if (!src || !dst || !idx) return PI_ERR_NULL;
     if (src_rows < 1 || dst_rows < 1 || row_bytes < 1) return PI_ERR_SHAPE;
     if (!al(idx, 4)) return PI_ERR_ALIGN;
@@ -547,6 +567,7 @@ pi_status pi_shard_neurons(const int32_t *order, int32_t n, int32_t shards, int3
 pi_status pi_rms_residual(const float *x, const float *y, int32_t batch, int32_t d_model, float *x_next,
                           pi_stream stream)
 {
+    Nvtx nv("pi_rms_residual");
     if (!x || !y || !x_next) return PI_ERR_NULL;
     if (batch < 1 || d_model < 1) return PI_ERR_SHAPE;
     if (!al(x, 4) || !al(y, 4) || !al(x_next, 4)) return PI_ERR_ALIGN;
@@ -555,6 +576,7 @@ pi_status pi_rms_residual(const float *x, const float *y, int32_t batch, int32_t
 
 pi_status pi_sync_status(void *ws, size_t ws_bytes, pi_stream stream)
 {
+    Nvtx nv("pi_sync_status");
     if (!ws) return PI_ERR_WORKSPACE;
     if (ws_bytes < sizeof(WsCtrl)) return PI_ERR_WORKSPACE;
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return PI_ERR_CUDA;

@@ -20,7 +20,7 @@ constexpr long long kSpinLimit = 1ll << 22;
 // First 256 bytes of a workspace.
 struct WsCtrl {
     unsigned err;           // ERR_* bits, cleared by pi_sync_status
-    unsigned spare;
+    unsigned poll_limit;    // polls of a cross-CTA wait before it gives up (0: kSpinLimit)
     unsigned done;          // scan: CTAs finished in the running launch
     unsigned epoch;         // scan: launch generation, tags the CTA status words
     unsigned long long bar_ctr;  // one-kernel layer step: grid-barrier arrivals (never reset)
@@ -188,6 +188,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, unsigned parity)
 #define PI_MBAR_SUSPEND_NS 10000u
 #endif
 
+// Poll limit of the cross-CTA waits of a launch: the control block's setting,
+// or kSpinLimit when it is 0.
+__device__ __forceinline__ long long poll_limit(const WsCtrl *c)
+{
+    const unsigned v = *reinterpret_cast<const volatile unsigned *>(&c->poll_limit);
+    return v ? (long long)v : kSpinLimit;
+}
+
 // Bounded wait for the phase with the given parity to complete (a bounded
 // number of polls, well under a second in total), then it raises
 // ERR_TIMEOUT and returns false.
@@ -218,6 +226,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// mbar_wait by all 32 lanes of a warp with one answer for the warp: true only
+// when every lane saw the phase complete, so that no lane leaves a loop of
+// warp-wide shuffles that the others stay in.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, unsigned parity, unsigned *err)
+{
+    const bool got = mbar_wait(bar, parity, err);
+    return __all_sync(0xffffffffu, got);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)

@@ -75,6 +75,7 @@ struct Tables {
     float redu[kUpRing][kNCW][2];
     int upcnt[kUpRing];
     unsigned long long seq;
+    int fail;           // set by any thread whose wait gave up; read after each CTA barrier
     int share_n;
     int count, total;
     unsigned qbase;     // queue mode: the queue slot of the range's k-th active neuron is qbase + k
@@ -125,15 +126,21 @@ __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
 // barrier before the call makes the other threads' writes part of this
 // thread's release).  Arrivals add to a 64-bit counter that is never reset;
 // the barrier is passed when the counter reaches `target` (a multiple of the
-// grid size derived from the launch sequence number).  Returns false on
-// timeout.
-__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long target, unsigned *err)
+// grid size derived from the launch sequence number).  Every CTA arrives
+// exactly once per barrier, also after a failure (`wait` false), so the
+// counter stays in step with the launch sequence.  The poll backs off with a
+// short sleep after the first few reads and gives up after `limit` polls
+// (ERR_TIMEOUT, returns false).
+__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long target, bool wait, long long limit,
+                             unsigned *err)
 {
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
-    for (long long i = 0; i < kSpinLimit; ++i) {
+    if (!wait) return false;
+    for (long long i = 0; i < limit; ++i) {
         unsigned long long v;
         asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
         if ((long long)(v - target) >= 0) return true;
+        if (i >= 16) __nanosleep(32);
     }
     atomicOr(err, ERR_TIMEOUT);
     return false;
@@ -162,6 +169,7 @@ struct FusedParams {
     unsigned *status;    // [G] active count of each CTA's range
     WsCtrl *ctrl;
     int d, F, r, act;
+    int queue;           // 1: FFN rows through the shared work queue (no ordered list)
     float tau;
     const uint8_t *pf[2];  // the next layer's predictor weights (or null), asked into L2
     size_t pf_bytes[2];
@@ -201,11 +209,12 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     const int rp1 = max(1, min(kMaxP1, (int)(stage_bytes / p1row)));  // P1 rows per job
     const int nP1 = (nP1r + rp1 - 1) / rp1;
     const int nP2 = (nR + kGroup - 1) / kGroup;
-    // No ordered active list requested: the FFN rows come from a shared work
-    // queue that every CTA feeds with its range's active neurons, so there is
-    // no second grid barrier, no prefix scan and no share lookup, and idle CTAs
-    // take rows from busy ones.
-    const bool qmode = !p.idx_out && !p.n_active;
+    // No ordered active list requested (and a layer narrow enough that the
+    // CTAs' share tables can hold every neuron, see launch_layer_b1): the FFN
+    // rows come from a shared work queue that every CTA feeds with its range's
+    // active neurons, so there is no second grid barrier, no prefix scan and
+    // no share lookup, and idle CTAs take rows from busy ones.
+    const bool qmode = p.queue != 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
@@ -215,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         mbar_init(&T.share_ready, 1);
         fence_mbar_init();
     }
+    if (threadIdx.x == 0) T.fail = 0;
     for (int i = threadIdx.x; i < kMaxShare; i += kThreads) T.state[i] = 0;
     for (int i = threadIdx.x; i < kUpRing; i += kThreads) T.upcnt[i] = 0;
     for (int i = threadIdx.x; i < nR; i += kThreads) {  // layer constants: no need to wait
@@ -233,9 +243,19 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         if (lane == 0) {
             int q = 0;
             bool failed = false;
+            volatile int *fail = &T.fail;
+            // a free stage for job qq; gives up early once a consumer has failed
+            // (its warps release no more stages)
             auto acquire = [&](int qq) -> bool {
+                if (qq < nstages) return true;
                 const int s = qq % nstages;
-                return qq < nstages || mbar_wait(&T.empty[s], (unsigned)((qq / nstages) - 1) & 1u, err);
+                const unsigned par = (unsigned)((qq / nstages) - 1) & 1u;
+                for (int i = 0; i < (1 << 16); ++i) {
+                    if (mbar_try_wait_sleep(&T.empty[s], par, PI_MBAR_SUSPEND_NS)) return true;
+                    if (*fail) return false;
+                }
+                atomicOr(err, ERR_TIMEOUT);
+                return false;
             };
             for (int i = 0; i < nP1 + nP2; ++i) {
                 if (i == min(nstages, nP1 + nP2)) {
@@ -272,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             // from the shared work queue
             if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
             int sn = failed ? 0 : T.share_n;
+            const long long plim = poll_limit(p.ctrl);  // the control block is the previous kernel's until now
 #ifndef PI_FUSED_PREFETCH_DOWN
 #define PI_FUSED_PREFETCH_DOWN 0
 #endif
@@ -297,6 +318,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             const unsigned par = (unsigned)T.seq & 1u, tag = (unsigned)T.seq + 1u;
             while (!failed) {
                 int kind, i = 0, j = 0;
+                if (*fail) {  // the consumers have stopped: issue nothing more
+                    failed = true;
+                    break;
+                }
                 if (ds < up && state[ds] != 0) {
                     const int stt = state[ds];
                     i = ds++;
@@ -306,9 +331,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 } else if (up >= sn && !exhausted) {
                     // take kQTake queue slots with one atomic; read the batch's
                     // remaining slots together; a slot is ready once its tag is
-                    // this launch's; a slot at or past the final tail ends the queue
+                    // this launch's; a slot at or past the final tail ends the queue.
+                    // A batch is claimed only while the share table has room for
+                    // all of it, so every claimed row is run; a CTA whose table is
+                    // that full takes no more (the host picks queue mode only when
+                    // the tables of all CTAs together hold every neuron)
                     if (pend < 0) {
-                        if (sn >= kMaxShare) {
+                        if (sn + kQTake > kMaxShare) {
                             exhausted = true;
                             continue;
                         }
@@ -327,13 +356,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     int took = 0;
 #pragma unroll
                     for (int k = 0; k < kQTake; ++k) {
-                        if (took != k || pk + k >= kQTake || sn >= kMaxShare) break;
+                        if (took != k || pk + k >= kQTake) break;
                         if ((unsigned)(ev[k] >> 32) != tag) break;
                         T.j[sn++] = (int)(unsigned)(ev[k] & 0xffffffffull);
                         ++took;
                     }
                     pk += took;
-                    if (pk == kQTake || sn >= kMaxShare) {
+                    if (pk == kQTake) {
                         pend = -1;
                         continue;
                     }
@@ -347,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                         pend = -1;
                         continue;
                     }
-                    if (++qspins < kSpinLimit) {
+                    if (++qspins < plim) {
                         __nanosleep(32);
                         continue;
                     }
@@ -424,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     const int t = threadIdx.x;
     pdl_wait();
     pdl_trigger();
+    const long long plim = poll_limit(p.ctrl);
     if (t == 0) T.seq = ld_volatile_u32(&p.ctrl->bar_seq);
 
     // this thread's float4 of y = b_down + residual (at most one per thread:
@@ -461,8 +491,16 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
         }
     }
+    // ok is warp-uniform between CTA barriers (every stage wait is decided for
+    // the whole warp) and CTA-uniform right after each of them (a failure
+    // anywhere in the CTA sets T.fail, read after the barrier)
     bool ok = true;
     int q = 0;
+    volatile int *fail = &T.fail;
+    auto cta_sync = [&]() {
+        named_bar_sync(1, kNCT);
+        ok = ok && *fail == 0;
+    };
 
     auto release = [&](int s) {
         __syncwarp();
@@ -472,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     // ---- 1. hidden layer: this CTA's P1 rows, rp1 rows per job ----
     for (int i = 0; i < nP1 && ok; ++i, ++q) {
         const int s = q % nstages;
-        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
+        if (!mbar_wait_warp(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
             ok = false;
+            *fail = 1;
             break;
         }
         const uint8_t *st = stages + (size_t)s * stage_bytes;
@@ -496,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         release(s);
     }
-    named_bar_sync(1, kNCT);
+    cta_sync();
     if (t < nP1r) {
         float z = 0.f;
 #pragma unroll
@@ -517,12 +556,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         p.ctrl->q_tail[qpar] = 0u;
         p.ctrl->q_done[qpar] = 0u;
     }
-    if (t == 0 && !grid_barrier(&p.ctrl->bar_ctr, base + (unsigned long long)G, err)) ok = false;
     if (t == 0) {
-        // every CTA has read this launch's sequence number: move it on
+        if (!grid_barrier(&p.ctrl->bar_ctr, base + (unsigned long long)G, ok, plim, err)) *fail = 1;
+        // every CTA has read this launch's sequence number: move it on (also
+        // after a failure, so the sequence stays in step with the counter)
         if (c == 0) atomicAdd(&p.ctrl->bar_seq, 1u);
     }
-    named_bar_sync(1, kNCT);
+    cta_sync();
     for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
     named_bar_sync(1, kNCT);
     // this lane's slices of h for the P2 rows, kept in registers (the first
@@ -547,13 +587,14 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         const int q0 = q;
         const int mr = min(kNCW, nstages);
         for (int i0 = 0; i0 < nP2; i0 += mr) {  // uniform trip count: every warp meets every barrier
-            if (i0 > 0) named_bar_sync(1, kNCT);
+            if (i0 > 0) cta_sync();
             const int i = i0 + warp;
             if (!ok || warp >= mr || i >= nP2) continue;
             const int qq = q0 + i;
             const int s = qq % nstages;
-            if (!mbar_wait(&T.full[s], (unsigned)(qq / nstages) & 1u, err)) {
+            if (!mbar_wait_warp(&T.full[s], (unsigned)(qq / nstages) & 1u, err)) {
                 ok = false;
+                *fail = 1;
                 continue;
             }
             const uint8_t *st = stages + (size_t)s * stage_bytes;
@@ -605,11 +646,12 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         q = q0 + nP2;
     }
-    named_bar_sync(1, kNCT);
+    cta_sync();
+    // after a failure no neuron is published (the logits are not valid)
     const int nw = (nR + 31) >> 5;
     for (int wd = warp; wd < nw; wd += kNCW) {
         const int row = wd * 32 + lane;
-        const bool on = row < nR && T.lg[row] > p.tau;
+        const bool on = ok && row < nR && T.lg[row] > p.tau;
         const unsigned bits = __ballot_sync(0xffffffffu, on);
         if (lane == 0) T.words[wd] = bits;
     }
@@ -677,9 +719,9 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     named_bar_sync(1, kNCT);
     if (t == 0) {
         p.status[c] = (unsigned)T.count;
-        if (!grid_barrier(&p.ctrl->bar_ctr, base + 2ull * (unsigned long long)G, err)) ok = false;
+        if (!grid_barrier(&p.ctrl->bar_ctr, base + 2ull * (unsigned long long)G, ok, plim, err)) *fail = 1;
     }
-    named_bar_sync(1, kNCT);
+    cta_sync();
     // every range's count -> exclusive prefix and total
     for (int i = t; i < G; i += kNCT) T.pref[i] = (int)ld_cg_int(reinterpret_cast<const int *>(p.status) + i);
     named_bar_sync(1, kNCT);
@@ -710,12 +752,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         if (t == 0) {
             T.total = total;
-            if (c == G - 1 && p.n_active) *p.n_active = total;
+            if (c == G - 1 && p.n_active && ok) *p.n_active = total;
         }
     }
     named_bar_sync(1, kNCT);
-    const int n = T.total;
-    if (p.idx_out) {  // this range's part of the ordered active list
+    // after a failure the counts are not this launch's: no list, no share
+    const int n = ok ? T.total : 0;
+    if (p.idx_out && ok) {  // this range's part of the ordered active list
         for (int i = t; i < T.count; i += kNCT) p.idx_out[T.pref[c] + i] = p.cand[j0 + i];
     }
     // this CTA's balanced share of the active list
@@ -743,7 +786,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     bool any = false;
     while (ok) {
         const int s = q % nstages;
-        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) break;
+        if (!mbar_wait_warp(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
+            *fail = 1;
+            break;
+        }
         const int4 job = T.job[s];
         if (job.x == kJobEnd) {
             release(s);
@@ -888,6 +934,10 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     p.r = a.r;
     p.act = a.act;
     p.tau = a.tau;
+    // queue mode needs every active neuron to fit the CTAs' share tables: a CTA
+    // takes no more queue rows once fewer than kQTake slots are left, so all
+    // CTAs together always hold at least (kMaxShare - kQTake + 1) rows each
+    p.queue = (!a.idx_out && !a.n_active && (long long)a.F <= (long long)(kMaxShare - kQTake + 1) * G) ? 1 : 0;
     for (int k = 0; k < 2; ++k) {
         p.pf[k] = static_cast<const uint8_t *>(a.pf[k]);
         p.pf_bytes[k] = a.pf[k] ? a.pf_bytes[k] : 0;

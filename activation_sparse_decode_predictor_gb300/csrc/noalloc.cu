@@ -7,17 +7,21 @@
 // Its workspace is one file-scope device array of fixed size.  The array lives
 // on every GPU that loads the library, from module load until the process
 // exits.  Host code may not hand the array's name to a kernel (on the host it
-// is only a stand-in symbol), so the first call on each device looks up the
-// array's device address with cudaGetSymbolAddress while that device is
-// current, and caches it.  That first call should therefore come before any
-// stream capture.  The call allocates nothing: no cudaMalloc, no cudaFree, no
-// allocating library routine.
+// is only a stand-in symbol), so every call looks up the array's device
+// address with cudaGetSymbolAddress while the caller's device is current (no
+// allocation; looking it up each time keeps a cudaDeviceReset between calls
+// harmless).  The first call on a device may load the library's device code,
+// so it should come before any stream capture.  No call allocates: no
+// cudaMalloc, no cudaFree, no allocating library routine.
 //
-// All calls on a device share the array and leave their contents in it.  The
-// scan state in it keeps itself consistent from call to call; the error word
-// is cleared at the start of each call.  Two calls that overlap on the GPU
-// (different streams, or different host threads without ordering) race on the
-// array and give wrong results.
+// All calls on a device share the array and leave their contents in it.  A
+// small kernel at the start of each call prepares it: it clears the error word,
+// and it zero-fills the whole region the layer uses when the layer's shape or
+// storage types differ from the previous call's on that device, or when the
+// previous call left a timeout in the error word (a wait that gave up can
+// leave the barrier and queue state out of step).  Two calls that overlap on
+// the GPU (different streams, or different host threads without ordering)
+// race on the array and give wrong results.
 #include <mutex>
 
 #include "internal.h"
@@ -33,21 +37,40 @@ constexpr int kStaticMaxDff = 65536;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
+struct LastShape {
+    bool valid;
+    int d_model, d_ff, rank, wtype, ptype;
+};
 std::mutex g_mu;
-void *g_addr[64] = {nullptr};
+LastShape g_last[64] = {};
 
-// Device address of g_static_ws on the current device (looked up once).
-pi_status static_ws(void **out)
+// One block: read the error word the previous call left, then clear the error
+// word, or zero-fill the first n16 16-byte words when asked to (reset) or when
+// that word holds a timeout.
+__global__ void k_static_prepare(uint4 *ws, size_t n16, int reset)
+{
+    __shared__ int wipe;
+    if (threadIdx.x == 0) {
+        const unsigned prev = *reinterpret_cast<volatile unsigned *>(ws);
+        wipe = reset || (prev & pi::ERR_TIMEOUT) != 0u;
+    }
+    __syncthreads();
+    if (!wipe) {
+        if (threadIdx.x == 0) *reinterpret_cast<unsigned *>(ws) = 0u;
+        return;
+    }
+    for (size_t i = threadIdx.x; i < n16; i += blockDim.x) ws[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Device address of g_static_ws on the current device, and the device ordinal.
+pi_status static_ws(void **out, int *dev_out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PI_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return PI_ERR_CUDA;
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return PI_ERR_CUDA;
+    *out = p;
+    *dev_out = dev;
     return PI_OK;
 }
 
@@ -58,16 +81,27 @@ extern "C" PI_API pi_status pi_ffn_layer_static(const pi_ffn_desc *desc, const f
                                                 pi_stream stream)
 {
     if (!desc) return PI_ERR_NULL;
+    if (desc->d_model < 8 || desc->d_ff < 1 || desc->rank < 0) return PI_ERR_SHAPE;
     if (desc->d_ff > kStaticMaxDff || desc->rank > PI_MAX_RANK) return PI_ERR_SHAPE;
     const pi::WsLayout L = pi::ws_layout(desc->d_model, desc->d_ff, desc->rank, 1);
     if (L.total > kStaticWsBytes) return PI_ERR_SHAPE;
     if (status_out && ((uintptr_t)status_out & 3)) return PI_ERR_ALIGN;
     void *ws = nullptr;
-    pi_status st = static_ws(&ws);
+    int dev = 0;
+    pi_status st = static_ws(&ws, &dev);
     if (st != PI_OK) return st;
     const cudaStream_t s = (cudaStream_t)stream;
-    // a fresh error word for this call; the scan state stays as the last call left it
-    if (cudaMemsetAsync(ws, 0, sizeof(unsigned), s) != cudaSuccess) return PI_ERR_CUDA;
+    int reset = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        LastShape &ls = g_last[dev];
+        const LastShape now = {true, desc->d_model, desc->d_ff, desc->rank, desc->wtype, desc->ptype};
+        reset = !(ls.valid && ls.d_model == now.d_model && ls.d_ff == now.d_ff && ls.rank == now.rank &&
+                  ls.wtype == now.wtype && ls.ptype == now.ptype);
+        ls = now;
+    }
+    k_static_prepare<<<1, 1024, 0, s>>>(static_cast<uint4 *>(ws), L.total / 16, reset);
+    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
     st = pi_ffn_layer(desc, x, 1, residual, y, idx, n_active, ws, L.total, stream);
     if (st != PI_OK) return st;
     if (status_out &&

@@ -3,13 +3,16 @@ HBM GB/s of the dominant kernel against the HBM roofline.
 
 One step = the whole hot path (predictor GEMVs, threshold + union, active-index
 compaction, gather up/gate projections, activation, scatter-accumulate down
-projection) for every decode token of one batch of synthetic tokens (256 for
-the default workload), token by token at batch 1, each token on the next of
-R rotating copies of the layer so the step's weight traffic (R x the layer)
-is far larger than L2, as consecutive layers of a real model would be.
+projection) for every decode token of one batch of synthetic tokens.
 
-Default workload: the ReLU-LLaMA-7B-shaped gated FFN layer (d_model 4096,
-d_ff 11008, fp16 weights, predictor rank 1024, ~90% Zipf-biased sparsity).
+Default workload: the OPT-175B-shaped stack of 12 non-gated ReLU FFN layers
+(d_model 12288, d_ff 49152, fp16 weights, predictor rank 1024, ~95%
+Zipf-biased sparsity), 128 decode tokens per step, each token through all 12
+distinct layers with the residual + RMS rescale between them, timed end to
+end; its 29 GB of weights are far larger than L2.  Single-layer workloads run
+each token on the next of R rotating copies of the layer, so a step's weight
+traffic (R x the layer) is far larger than L2, as consecutive layers of a real
+model would be.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -50,9 +53,9 @@ KERNEL_SOURCES = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="llama7b-reglu-fp16", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="opt175b-relu-fp16-stack12", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--replicas", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle sample")
@@ -194,9 +197,45 @@ def q4_dequant_torch(blob, rows, cols):
     return (q * scales).reshape(rows, cols)
 
 
+def top_share(counts, frac=0.26):
+    """Share of all firings carried by the `frac` most frequently firing
+    neurons (the power-law locality statistic of the pages)."""
+    c = np.sort(np.asarray(counts, dtype=np.float64))[::-1]
+    k = max(1, int(round(frac * c.size)))
+    return float(c[:k].sum() / max(1.0, c.sum()))
+
+
+def hot_first(w, L0, dev):
+    """Offline profiling pass: w.profile_tokens synthetic tokens (a token stream
+    of their own) through pi_fire_counts on the layer as generated, the
+    hot-first order from pi_hot_first_perm, then every per-neuron array (rows of
+    w_up / w_gate / w_down / p2, entries of b_act / p_bias) permuted with
+    pi_permute_rows.  Returns the permuted layer and statistics of the order."""
+    F = w.d_ff
+    lay = B.Layer.from_dict(L0)
+    Xp = synth.workload_tokens(w, n=w.profile_tokens, device=f"cuda:{dev}", stream=1)
+    counts = torch.zeros(F, dtype=torch.int32, device=Xp.device)
+    B.pi_fire_counts(lay, Xp, counts)
+    c = counts.cpu().numpy()
+    perm = B.pi_hot_first_perm(c)
+    perm_d = torch.from_numpy(perm).to(Xp.device)
+    out = dict(L0)
+    for k in ("w_up", "w_gate", "w_down", "p2", "b_act", "p_bias"):
+        if L0.get(k) is not None:
+            out[k] = B.pi_permute_rows(L0[k], perm_d)
+    torch.cuda.synchronize()
+    cs = c[perm].astype(np.float64)
+    stats = {"profile_tokens": int(w.profile_tokens),
+             "first_quarter_share_profile": float(cs[: F // 4].sum() / max(1.0, cs.sum()))}
+    return out, perm, stats
+
+
 def setup_ours(w, replicas, dev):
     torch.cuda.set_device(dev)
     L0 = synth.workload_layer(w, 0, device=f"cuda:{dev}")
+    perm_stats = None
+    if w.permute:
+        L0, _, perm_stats = hot_first(w, L0, dev)
     if w.wtype == "q4_0":
         # the generator returns fp16 matrices; store them as Q4_0 with the library's quantiser
         for k in ("w_up", "w_gate", "w_down"):
@@ -214,14 +253,15 @@ def setup_ours(w, replicas, dev):
     for k in range(replicas):
         reps[k][1].set_next(reps[(k + 1) % replicas][1])
     X = synth.workload_tokens(w, device=f"cuda:{dev}")
-    return L0, reps, X
+    return L0, reps, X, perm_stats
 
 
 def active_stats(w, L0, layer, X, ws, ws1, batch):
     """Per group of `batch` tokens: predicted (union) active count and the count
     of those rows with a non-zero activation for some token of the group; per
-    token: recall and precision of the predictor against the true ReLU mask.
-    Uses the library for the predictions and torch only to count."""
+    token: recall and precision of the predictor against the true ReLU mask,
+    and the true mask itself.  Uses the library for the predictions and torch
+    only to count."""
     T = X.shape[0]
     G = T // batch
     F = w.d_ff
@@ -250,7 +290,19 @@ def active_stats(w, L0, layer, X, ws, ws1, batch):
     inter = (own & true).sum(dim=1).float()
     rec = float((inter / true.sum(dim=1).clamp(min=1)).mean())
     prec = float((inter / own.sum(dim=1).clamp(min=1)).mean())
-    return idx, n, np.array(n_pred), np.array(n_down), rec, prec, float(true.float().mean())
+    return dict(idx=idx, n=n, n_pred=np.array(n_pred), n_down=np.array(n_down), recall=rec, precision=prec,
+                true_density=float(true.float().mean()), true=true)
+
+
+def true_lists(true):
+    """Ascending true-active lists [T, F] (int32, device) and their lengths [T]."""
+    T, F = true.shape
+    idx = torch.zeros(T, F, dtype=torch.int32, device=true.device)
+    n = true.sum(dim=1).to(torch.int32)
+    for t in range(T):
+        nz = torch.nonzero(true[t]).flatten().to(torch.int32)
+        idx[t, : nz.numel()] = nz
+    return idx, n
 
 
 def capture(fn, stream):
@@ -281,6 +333,13 @@ def time_graph(g, steps, warmup, stream, barrier=None):
         if barrier:
             barrier()
     return e0.elapsed_time(e1)  # ms
+
+
+def roofline_obj(kernel, achieved, peak, peak_src, traffic, **extra):
+    r = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
+         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src}
+    r.update(extra)
+    return r
 
 
 # ------------------------------------------------------------------------------------ CPU oracle
@@ -315,7 +374,6 @@ def host_layer(L0, w=None):
     return H
 
 
-# ------------------------------------------------------------------------------------ arms
 def oracle_stack_sample(w, olays, X_host, budget_s):
     """Time the oracle through every layer of a stack (predictor, compaction,
     sparse FFN, residual + rescale) on as many tokens as fit the budget;
@@ -348,64 +406,84 @@ def oracle_layer(w, H):
                         b_down=H["b_down"], p1=H["p1"], p2=H["p2"], p_bias=H["p_bias"], threshold=H["threshold"])
 
 
+# ------------------------------------------------------------------------------------ arms
+def reference_layers(w):
+    """The workload's layers as host arrays for the oracle, drawn by the same
+    seeded generator as the GPU arm (on the GPU when there is one, so both arms
+    see the same numbers).  A hot-first neuron order is not applied here: it
+    only renames neurons, and the oracle's work per token does not depend on
+    the order."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    out = []
+    for l in range(w.layers):
+        L = synth.workload_layer(w, l, device=dev)
+        out.append(oracle_layer(w, host_layer(L, w)))
+        del L
+    X = synth.workload_tokens(w, device=dev).cpu().numpy()
+    return out, X
+
+
 def run_reference(args, w):
+    """The reference arm: the CPU oracle as it stands, single-threaded, on a
+    bounded sample of the same workload per step.  ms_per_step is the wall time
+    of the sample each step actually ran (tokens_per_step of them)."""
     ws_, rank, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     oracle.build()
-    if w.layers > 1 and not args.one_layer:
-        olays = [oracle_layer(w, host_layer(synth.workload_layer(w, l, device="cpu"), w)) for l in range(w.layers)]
-        X = synth.workload_tokens(w, device="cpu").numpy()
-        per_step = []
-        budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-        ntok = 0
-        for s in range(args.warmup + args.steps):
-            us, ntok = oracle_stack_sample(w, olays, X[(s * 7) % X.shape[0]:], budget)
-            if s >= args.warmup:
-                per_step.append(us)
-        value = float(np.median(per_step))
-        line = {"impl": "reference", "metric": "us_per_ffn_layer_per_token", "value": value,
-                "unit": "us/layer/token", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": value * w.tokens * w.layers / 1000.0, "higher_is_better": False, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name, "d_model": w.d_model, "d_ff": w.d_ff, "rank": w.rank,
-                           "gated": w.gated, "weights": w.wtype, "batch": 1, "layers": w.layers,
-                           "sparsity": w.sparsity},
-                "cpu_baseline": {"value": value, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
-                                 "sample": f"{ntok} token(s) per step through all {w.layers} layers, "
-                                           "single-threaded C, fp64"},
-                "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-                "cpu_dense": {"value": oracle_dense_us(olays[0], X[0]), "unit": "us/layer/token",
-                              "sample": "1 token through layer 0, every neuron, single-threaded C oracle, fp64"}}
-        print(json.dumps(line))
-        return 0
-    L0 = synth.workload_layer(w, 0, device="cpu")
-    H = host_layer(L0, w)
-    X = synth.workload_tokens(w, device="cpu").numpy()
-    per_step = []
-    tokens_per_sample = None
+    stack = w.layers > 1 and not args.one_layer
+    if not stack and w.layers > 1:
+        w = synth.Workload(**{**w.__dict__, "layers": 1})
+    olays, X = reference_layers(w)
     budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    per_step, wall_ms, ntoks = [], [], []
     for s in range(args.warmup + args.steps):
-        us, ntok = oracle_sample(w, H, X[(s * 7) % X.shape[0]:], budget)
+        t0 = time.perf_counter()
+        if stack:
+            us, ntok = oracle_stack_sample(w, olays, X[(s * 7) % X.shape[0]:], budget)
+        else:
+            us, ntok = oracle_sample_layer(olays[0], X[(s * 7) % X.shape[0]:], budget)
         if s >= args.warmup:
             per_step.append(us)
-            tokens_per_sample = ntok
+            wall_ms.append((time.perf_counter() - t0) * 1000.0)
+            ntoks.append(ntok)
     value = float(np.median(per_step))
+    what = (f"token(s) per step through all {w.layers} layers (predictor, compaction, sparse FFN, residual + "
+            "rescale)" if stack else "token(s) per step through one layer (predictor, compaction, sparse FFN)")
     line = {"impl": "reference", "metric": "us_per_ffn_layer_per_token", "value": value,
             "unit": "us/layer/token", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": value * w.tokens / 1000.0, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "d_model": w.d_model, "d_ff": w.d_ff, "rank": w.rank,
-                       "gated": w.gated, "weights": w.wtype, "batch": w.batch, "sparsity": w.sparsity},
+            "ms_per_step": float(np.median(wall_ms)), "tokens_per_step": int(np.median(ntoks)),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {**workload_config(w, 1, stack), "hot_first_order": False},
             "cpu_baseline": {"value": value, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
-                             "sample": f"{tokens_per_sample} token(s) per step through one layer (predictor, "
-                                       "compaction, sparse FFN), single-threaded C, fp64"},
+                             "sample": f"{int(np.median(ntoks))} {what}, single-threaded C, fp64"},
             "e2e": {"value": value, "unit": "us/layer/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "cpu_dense": {"value": oracle_dense_us(oracle_layer(w, H), X[0]), "unit": "us/layer/token",
-                          "sample": "1 token, every neuron, single-threaded C oracle, fp64"}}
+            "cpu_dense": {"value": oracle_dense_us(olays[0], X[0]), "unit": "us/layer/token",
+                          "sample": "1 token through the first layer, every neuron, single-threaded C oracle, fp64"}}
     print(json.dumps(line))
     return 0
+
+
+def oracle_sample_layer(olay, X_host, budget_s):
+    import oracle
+    t0 = time.perf_counter()
+    done = 0
+    while done < X_host.shape[0] and (done == 0 or time.perf_counter() - t0 < budget_s):
+        _, _, m = oracle.predict(olay, X_host[done])
+        oracle.sparse_ffn(olay, X_host[done], oracle.compact(m))
+        done += 1
+    return (time.perf_counter() - t0) / done * 1e6, done
+
+
+def workload_config(w, batch, stack):
+    c = {"workload": w.name, "d_model": w.d_model, "d_ff": w.d_ff, "rank": w.rank, "gated": w.gated,
+         "weights": w.wtype, "accumulate": "f32", "batch": batch, "sparsity": w.sparsity,
+         "hot_first_order": bool(w.permute)}
+    if stack:
+        c["layers"] = w.layers
+    return c
 
 
 def run_ours(args, w):
@@ -419,7 +497,7 @@ def run_ours(args, w):
     dev = local
     torch.cuda.set_device(dev)
     B.lib()
-    L0, reps, X = setup_ours(w, args.replicas, dev)
+    L0, reps, X, perm_stats = setup_ours(w, args.replicas, dev)
     if args.tokens:
         X = X[:args.tokens].contiguous()
     bsz = args.batch or w.batch
@@ -435,11 +513,11 @@ def run_ours(args, w):
     Yg = [Y[gi * bsz:(gi + 1) * bsz] if bsz > 1 else Y[gi] for gi in range(G)]
 
     # statistics of the active sets (outside any timed region)
-    idx_all, n_all, n_pred, n_down, recall, precision, true_density = active_stats(w, L0, reps[0][1], X, ws, ws1,
-                                                                                   bsz)
-    pred_b, ffn_b = needed_bytes(w, n_pred, n_down, bsz)
+    S = active_stats(w, L0, reps[0][1], X, ws, ws1, bsz)
+    pred_b, ffn_b = needed_bytes(w, S["n_pred"], S["n_down"], bsz)
     bytes_grp = pred_b + ffn_b                       # per group, arrays
     mean_bytes = float(np.mean(bytes_grp)) / bsz     # per token
+    fire = S["true"].sum(dim=0).cpu().numpy()
 
     def step():
         for gi in range(G):
@@ -460,7 +538,9 @@ def run_ours(args, w):
                               "device_status": B.pi_sync_status(ws)}))
         return 0
 
-    # the dominant kernel alone: the sparse FFN on the predicted lists (same rotation)
+    # the sparse FFN alone on the predicted lists (same rotation), and the predictor alone
+    idx_all, n_all = S["idx"], S["n"]
+
     def sparse_only():
         for gi in range(G):
             B.pi_sparse_ffn(reps[gi % len(reps)][1], Xg[gi], idx_all[gi], n_all[gi:gi + 1], Yg[gi], ws=ws)
@@ -479,12 +559,34 @@ def run_ours(args, w):
     ffn_gbs = float(np.mean(ffn_b)) / (us_sp * 1e-6) / 1e9
     pred_gbs = float(pred_b) / (us_pr * 1e-6) / 1e9
     layer_gbs = mean_bytes / (us_tok * world * 1e-6) / 1e9
+    kernels = {"per": "token" if bsz == 1 else f"group of {bsz} tokens",
+               "predict_us": us_pr, "predict_gbs": pred_gbs, "predict_frac": pred_gbs / peak,
+               "sparse_ffn_us": us_sp, "sparse_ffn_gbs": ffn_gbs, "sparse_ffn_frac": ffn_gbs / peak,
+               "layer_gbs": layer_gbs, "layer_frac": layer_gbs / peak}
+
+    if bsz == 1:
+        # measurement mode (i): the sparse FFN alone on the TRUE active lists, at
+        # exactly the generator's sparsity (kernel roofline without the predictor)
+        tidx, tn = true_lists(S["true"])
+
+        def sparse_true():
+            for t in range(T):
+                B.pi_sparse_ffn(reps[t % len(reps)][1], X[t], tidx[t], tn[t:t + 1], Y[t], ws=ws)
+
+        g_tr = capture(sparse_true, stream)
+        ms_tr = time_graph(g_tr, ksteps, args.warmup, stream) / ksteps
+        us_tr = ms_tr * 1000.0 / T
+        n_true = tn.cpu().numpy()
+        tr_b = float(np.mean(needed_bytes(w, n_true, n_true, 1)[1]))
+        kernels.update({"true_mask_sparse_ffn_us": us_tr, "true_mask_sparse_ffn_gbs": tr_b / (us_tr * 1e-6) / 1e9,
+                        "true_mask_sparse_ffn_frac": tr_b / (us_tr * 1e-6) / 1e9 / peak,
+                        "true_mask_n_mean": float(np.mean(n_true))})
 
     # end to end through the public API: pinned host tokens in, outputs back
     Xh = X.cpu().pin_memory()
     Yh = torch.empty(T, d, dtype=torch.float32).pin_memory()
     Xd = torch.empty_like(X)
-    e2e_steps = max(3, args.steps // 20)
+    e2e_steps = max(3, args.steps // 4)
     with torch.cuda.stream(stream):
         Xdg = [Xd[gi * bsz:(gi + 1) * bsz] if bsz > 1 else Xd[gi] for gi in range(G)]
 
@@ -509,7 +611,7 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         oracle.build()
-        H0 = host_layer(L0) if w.wtype != "q4_0" else host_layer(synth.workload_layer(w, 0, device="cpu"), w)
+        H0 = host_layer(L0) if w.wtype != "q4_0" else host_layer(synth.workload_layer(w, 0, device=X.device), w)
         us_cpu, ntok = oracle_sample(w, H0, X.cpu().numpy(), args.cpu_seconds)
         cpu = {"value": us_cpu, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
                "sample": f"first {ntok} of {T} tokens through one layer (predictor, compaction, sparse FFN), "
@@ -518,40 +620,43 @@ def run_ours(args, w):
     if bsz == 1:
         # one kernel per token and layer: the whole step is k_layer_b1 back to back
         launches_per_group = 1
-        roofline = {"bound": "hbm", "kernel": "k_layer_b1 (pi_ffn_layer)", "achieved": layer_gbs,
-                    "traffic": committed_traffic("k_layer_b1", w.name)}
+        roofline = roofline_obj("k_layer_b1 (pi_ffn_layer)", layer_gbs, peak, peak_src,
+                                committed_traffic("k_layer_b1", w.name))
+        roofline_layer = None
     else:
         # predictor (2 kernels) + k_union_prep + k_union_up + k_union_down per group
-        launches_per_group = 5
-        roofline = {"bound": "hbm", "kernel": "k_union_prep + k_union_up + k_union_down (pi_sparse_ffn)",
-                    "achieved": ffn_gbs, "traffic": committed_traffic("k_union", f"{w.name}_b{bsz}")}
-    roofline.update({"peak": peak, "unit": "GB/s", "frac": roofline["achieved"] / peak, "peak_source": peak_src})
+        launches_per_group = 8
+        roofline = roofline_obj("k_union_prep + k_union_up + k_union_down (pi_sparse_ffn)", ffn_gbs, peak, peak_src,
+                                committed_traffic("k_union", f"{w.name}_b{bsz}"))
+        # the whole layer, predictor bytes included, over the timed step
+        roofline_layer = roofline_obj("pi_ffn_layer (predictor + compaction + union FFN)", layer_gbs, peak, peak_src,
+                                      None)
 
     if rank == 0:
+        cfg = workload_config(w, bsz, False)
+        cfg.update({"tokens_per_step": T, "layer_replicas": len(reps),
+                    "l2": f"inputs larger than L2: {len(reps)} rotating layer copies, "
+                          f"{len(reps) * mean_bytes / 1e6:.0f} MB needed bytes per rotation",
+                    "n_active_mean": float(np.mean(S["n_pred"])), "n_nonzero_mean": float(np.mean(S["n_down"])),
+                    "true_density": S["true_density"], "predictor_recall": S["recall"],
+                    "predictor_precision": S["precision"], "top26_firing_share": top_share(fire),
+                    "needed_bytes_per_token": mean_bytes, "parallelism": f"replicas x{world}"})
+        if perm_stats:
+            cfg["hot_first"] = perm_stats
+            cfg["hot_first"]["first_quarter_share_decode"] = float(fire[: w.d_ff // 4].sum() / max(1, fire.sum()))
         line = {
             "metric": "us_per_ffn_layer_per_token", "value": us_tok, "unit": "us/layer/token", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.wtype == "f16" else w.wtype,
-            "data": "synthetic",
-            "config": {"workload": w.name, "d_model": d, "d_ff": w.d_ff, "rank": w.rank, "gated": w.gated,
-                       "weights": w.wtype, "accumulate": "f32", "batch": bsz, "tokens_per_step": T,
-                       "sparsity": w.sparsity, "layer_replicas": len(reps),
-                       "l2": f"inputs larger than L2: {len(reps)} rotating layer copies, "
-                             f"{len(reps) * mean_bytes / 1e6:.0f} MB needed bytes per rotation",
-                       "n_active_mean": float(np.mean(n_pred)), "n_nonzero_mean": float(np.mean(n_down)),
-                       "true_density": true_density, "predictor_recall": recall, "predictor_precision": precision,
-                       "needed_bytes_per_token": mean_bytes, "parallelism": f"replicas x{world}"},
-            "roofline": roofline,
-            "kernels": {"per": "token" if bsz == 1 else f"group of {bsz} tokens",
-                        "predict_us": us_pr, "predict_gbs": pred_gbs, "predict_frac": pred_gbs / peak,
-                        "sparse_ffn_us": us_sp, "sparse_ffn_gbs": ffn_gbs, "layer_gbs": layer_gbs,
-                        "layer_frac": layer_gbs / peak},
+            "data": "synthetic", "config": cfg, "roofline": roofline, "kernels": kernels,
             "e2e": {"value": us_e2e, "unit": "us/layer/token", "h2d_bytes_per_step": int(Xh.numel() * 4),
                     "d2h_bytes_per_step": int(Yh.numel() * 4), "path": "pi_ffn_layer per group, direct calls"},
             "gpu_launches": launches_per_group * G * args.steps,
             "clocks": clk.summary(),
             "device_status": st,
         }
+        if roofline_layer:
+            line["roofline_layer"] = roofline_layer
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line))
@@ -566,7 +671,9 @@ def run_stack(args, w):
     through `w.layers` distinct layers, each layer's output plus its input
     rescaled by pi_rms_residual into the next layer's input, and the whole token
     is timed end to end.  Metric: us per layer per token (step time / tokens /
-    layers; the glue kernel is part of it)."""
+    layers; the glue kernel is part of it).  The roofline's dominant kernel,
+    k_layer_b1, is also timed alone: the same layer calls back to back on the
+    recorded inputs of every layer."""
     world, rank, local = dist_env()
     barrier = None
     if world > 1:
@@ -610,13 +717,17 @@ def run_stack(args, w):
     for t in range(T):
         token(X[t], Xout[t], record=[Xl[l, t] for l in range(nl)])
     torch.cuda.synchronize()
-    n_pred, n_down, recs, precs = [], [], [], []
+    n_pred, n_down, recs, precs, dens, fire = [], [], [], [], [], []
+    trues = []
     for l in range(nl):
-        _, _, npl, ndl, rec, prec, _ = active_stats(w, Ls[l], lays[l], Xl[l], ws, ws, 1)
-        n_pred.append(npl)
-        n_down.append(ndl)
-        recs.append(rec)
-        precs.append(prec)
+        S = active_stats(w, Ls[l], lays[l], Xl[l], ws, ws, 1)
+        n_pred.append(S["n_pred"])
+        n_down.append(S["n_down"])
+        recs.append(S["recall"])
+        precs.append(S["precision"])
+        dens.append(S["true_density"])
+        fire.append(S["true"].sum(dim=0).cpu().numpy())
+        trues.append(S["true"])
     n_pred, n_down = np.concatenate(n_pred), np.concatenate(n_down)
     pred_b, ffn_b = needed_bytes(w, n_pred, n_down, 1)
     mean_bytes = float(np.mean(pred_b + ffn_b))  # per token and layer
@@ -628,6 +739,40 @@ def run_stack(args, w):
     us_tok = whole_job_us_per_token(ms_step, T * nl, world)  # per layer per token
     layer_gbs = mean_bytes / (us_tok * world * 1e-6) / 1e9
     peak, peak_src = measured_peaks()
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": "us_per_ffn_layer_per_token", "value": us_tok, "unit": "us/layer/token",
+                              "quick": True, "workload": w.name, "tokens_per_step": T, "layer_gbs": layer_gbs,
+                              "device_status": B.pi_sync_status(ws)}))
+        return 0
+
+    # the dominant kernel alone: every layer's k_layer_b1 on its recorded input, back to back
+    ksteps = max(4, args.steps // 4)
+
+    def kernel_only():
+        for t in range(T):
+            for l in range(nl):
+                B.pi_ffn_layer(lays[l], Xl[l, t], ya, ws=ws)
+
+    g_k = capture(kernel_only, stream)
+    ms_k = time_graph(g_k, ksteps, min(args.warmup, 3), stream) / ksteps
+    us_k = ms_k * 1000.0 / (T * nl)
+    k_gbs = mean_bytes / (us_k * 1e-6) / 1e9
+
+    # measurement mode (i): the sparse FFN alone on every layer's TRUE active lists
+    tl = [true_lists(tr) for tr in trues]
+
+    def sparse_true():
+        for t in range(T):
+            for l in range(nl):
+                B.pi_sparse_ffn(lays[l], Xl[l, t], tl[l][0][t], tl[l][1][t:t + 1], ya, ws=ws)
+
+    g_tr = capture(sparse_true, stream)
+    ms_tr = time_graph(g_tr, ksteps, min(args.warmup, 3), stream) / ksteps
+    us_tr = ms_tr * 1000.0 / (T * nl)
+    n_true = np.concatenate([x[1].cpu().numpy() for x in tl])
+    tr_b = float(np.mean(needed_bytes(w, n_true, n_true, 1)[1]))
+    del tl
 
     # end to end: pinned host tokens in, the stack's outputs back
     Xh = X.cpu().pin_memory()
@@ -659,24 +804,35 @@ def run_stack(args, w):
         cpu = {"value": us_cpu, "unit": "us/layer/token", "cores": 1, "kind": "oracle",
                "sample": f"first {done} of {T} tokens through all {nl} layers (predictor, compaction, sparse FFN, "
                          "residual + rescale), single-threaded C oracle, fp64"}
+        del olays
 
     if rank == 0:
+        fire_all = np.concatenate(fire)
+        cfg = workload_config(w, 1, True)
+        cfg.update({"tokens_per_step": T,
+                    "l2": f"inputs larger than L2: {nl} distinct layers, "
+                          f"{nl * mean_bytes / 1e6:.0f} MB needed bytes per token",
+                    "n_active_mean": float(np.mean(n_pred)), "n_nonzero_mean": float(np.mean(n_down)),
+                    "true_density_per_layer": [round(x, 4) for x in dens],
+                    "predictor_recall": float(np.mean(recs)), "predictor_precision": float(np.mean(precs)),
+                    "top26_firing_share": float(np.mean([top_share(f) for f in fire])),
+                    "needed_bytes_per_token_layer": mean_bytes, "parallelism": f"replicas x{world}"})
+        del fire_all
         line = {
             "metric": "us_per_ffn_layer_per_token", "value": us_tok, "unit": "us/layer/token", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.wtype == "f16" else w.wtype,
-            "data": "synthetic",
-            "config": {"workload": w.name, "d_model": d, "d_ff": w.d_ff, "rank": w.rank, "gated": w.gated,
-                       "weights": w.wtype, "accumulate": "f32", "batch": 1, "layers": nl, "tokens_per_step": T,
-                       "sparsity": w.sparsity,
-                       "l2": f"inputs larger than L2: {nl} distinct layers, "
-                             f"{nl * mean_bytes / 1e6:.0f} MB needed bytes per token",
-                       "n_active_mean": float(np.mean(n_pred)), "n_nonzero_mean": float(np.mean(n_down)),
-                       "predictor_recall": float(np.mean(recs)), "predictor_precision": float(np.mean(precs)),
-                       "needed_bytes_per_token_layer": mean_bytes, "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "k_layer_b1 (pi_ffn_layer; glue kernel included in the time)",
-                         "achieved": layer_gbs, "peak": peak, "unit": "GB/s", "frac": layer_gbs / peak,
-                         "traffic": None, "peak_source": peak_src},
+            "data": "synthetic", "config": cfg,
+            "roofline": roofline_obj("k_layer_b1 (pi_ffn_layer), timed alone back to back on the stack's inputs",
+                                     k_gbs, peak, peak_src, committed_traffic("k_layer_b1", w.name),
+                                     launch_us=us_k),
+            "roofline_layer": roofline_obj("stack end to end (k_layer_b1 + glue kernel)", layer_gbs, peak, peak_src,
+                                           None),
+            "kernels": {"per": "layer and token", "layer_kernel_us": us_k, "layer_kernel_gbs": k_gbs,
+                        "layer_kernel_frac": k_gbs / peak, "step_us_per_layer": us_tok,
+                        "true_mask_sparse_ffn_us": us_tr, "true_mask_sparse_ffn_gbs": tr_b / (us_tr * 1e-6) / 1e9,
+                        "true_mask_sparse_ffn_frac": tr_b / (us_tr * 1e-6) / 1e9 / peak,
+                        "true_mask_n_mean": float(np.mean(n_true))},
             "e2e": {"value": us_e2e, "unit": "us/layer/token", "h2d_bytes_per_step": int(Xh.numel() * 4),
                     "d2h_bytes_per_step": int(Yh.numel() * 4), "path": "pi_ffn_layer + pi_rms_residual per layer"},
             "gpu_launches": 2 * nl * T * args.steps,

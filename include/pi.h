@@ -141,7 +141,12 @@ PI_API const char *pi_status_str(int32_t status);
  * keep it consistent themselves.  One workspace serves any sequence of calls
  * on the same stream for descriptors of the same d_model, d_ff, rank and a
  * batch no larger than the one it was sized for; calls that overlap in time
- * (other streams) need separate workspaces.
+ * (other streams) need separate workspaces.  After a call that reported
+ * PI_ERR_TIMEOUT the workspace must be zero-filled again before its next use.
+ * Bytes 4..7 of the workspace (a uint32) may be set by the caller: the number
+ * of polls after which a wait of one CTA on others (a grid barrier, the work
+ * queue) gives up; 0, the zero-filled default, means about 4 million polls
+ * (seconds).  A smaller value makes a lost wait fail faster.
  */
 PI_API size_t pi_workspace_bytes(const pi_ffn_desc *desc, int32_t batch);
 
@@ -203,8 +208,10 @@ PI_API pi_status pi_sparse_ffn(const pi_ffn_desc *desc, const float *x, int32_t 
  * resident at once.  If other streams or processes hold SMs long enough, its
  * bounded waits give up: PI_ERR_TIMEOUT from pi_sync_status, and y is not
  * valid.  With idx / n_active NULL the FFN rows are spread over the CTAs
- * dynamically; otherwise the ascending list is also written, which costs one
- * more grid-wide synchronisation.
+ * dynamically (for d_ff up to 509 x the number of SMs; wider layers take the
+ * next path); otherwise the ascending list is also written, which costs one
+ * more grid-wide synchronisation.  Every predicted neuron is computed in both
+ * cases.
  */
 PI_API pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual,
                        float *y, int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes,
@@ -327,13 +334,17 @@ PI_API pi_status pi_sync_status(void *ws, size_t ws_bytes, pi_stream stream);
  * Scratch space is a fixed file-scope device array of 1088 KiB inside the
  * library, present on every GPU that loads it until the process exits.  Limits:
  * d_ff <= 65536 and rank <= PI_MAX_RANK; larger layers return PI_ERR_SHAPE.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Nothing is allocated by any call.
+ * Every call looks up the array's device address on the current device (no
+ * allocation); the first call on a device may load the library's device code,
+ * so make it before any stream capture.  Nothing is allocated by any call.
  *
- * All calls share the array and it keeps the last call's contents; each call
- * clears its error word first.  Calls that overlap on the GPU (other streams
- * or unordered host threads) race on it and give wrong results.
+ * All calls share the array and it keeps the last call's contents.  Each call
+ * first clears the error word, and zero-fills the part of the array the layer
+ * uses when d_model, d_ff, rank, wtype or ptype differ from the previous
+ * call's on that device or when the previous call's bounded wait gave up, so
+ * layers of different shapes may alternate and a timeout needs no action from
+ * the caller.  Calls that overlap on the GPU (other streams or unordered host
+ * threads) race on the array and give wrong results.
  *   x, residual, y, idx, n_active: as in pi_ffn_layer with batch 1 (idx and
  *   n_active may both be NULL).
  *   status_out: device int32 [1] or NULL; receives the device error bits of

@@ -441,3 +441,49 @@ def test_queue_mode_matches_ordered_mode(wtype, gated, sparsity):
         y_ref = oracle.sparse_ffn(olay, X[t], res)
         assert_ffn_close(y1.cpu().numpy(), y_ref, what=f"ordered {wtype} gated={gated} t={t}")
         assert_ffn_close(y2.cpu().numpy(), y_ref, what=f"queue {wtype} gated={gated} t={t}")
+
+
+def _sm_count():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+@pytest.mark.parametrize("which,gated,density", [("queue_max", False, 1.0), ("queue_max", True, 0.85),
+                                                 ("queue_mid", False, 1.0), ("ordered_only", False, 1.0),
+                                                 ("ordered_only", True, 0.9)])
+def test_near_dense_wide_layer_runs_every_neuron(which, gated, density):
+    """Near-dense tokens on the widest layers the one-kernel step accepts, where
+    one CTA must run about 500 rows.  Without a list asked for, the rows go
+    through the shared work queue up to 509 rows per SM (every CTA's share table
+    then holds all of them); above that the step uses the ordered list.  Every
+    predicted neuron must be run in both cases, and the ordered list must be
+    exact.  The mask is fixed by the predictor's output bias (+-1e4 against
+    logits of order 1), so it is known without any rounding question."""
+    G = _sm_count()
+    F = {"queue_max": 509 * G, "queue_mid": 470 * G + 13, "ordered_only": 512 * G - 21}[which]
+    d, r = 256, 64
+    L = synth.make_layer(d, F, r, gated=gated, wtype="f16", sparsity=0.5, predictor="random", seed=F + gated,
+                         device="cuda")
+    on = np.random.default_rng(F + 1).random(F) < density
+    L["p_bias"] = torch.from_numpy(np.where(on, 1e4, -1e4).astype(np.float32)).cuda()
+    lay, olay, H = make_pair(L)
+    X = synth.tokens(2, d, 91).numpy()
+    ws = None
+    for t in range(2):
+        _, _, M = oracle.predict(olay, X[t])
+        assert np.array_equal(M.astype(bool), on)
+        ref_idx = oracle.compact(M)
+        y_ref = oracle.sparse_ffn(olay, X[t], ref_idx)
+        x = _cuda(X[t])
+        idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+        n = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y1 = torch.empty(d, dtype=torch.float32, device="cuda")
+        ws = B.pi_ffn_layer(lay, x, y1, idx=idx, n_active=n, ws=ws)
+        y2 = torch.empty(d, dtype=torch.float32, device="cuda")
+        B.pi_ffn_layer(lay, x, y2, ws=ws)
+        y3 = torch.empty(d, dtype=torch.float32, device="cuda")
+        B.pi_ffn_layer(lay, x, y3, ws=ws)                      # the queue counters alternate by launch
+        assert B.pi_sync_status(ws) == 0
+        assert int(n.item()) == ref_idx.size
+        assert np.array_equal(idx.cpu().numpy()[: ref_idx.size], ref_idx)
+        for y, mode in ((y1, "ordered"), (y2, "no list"), (y3, "no list, again")):
+            assert_ffn_close(y.cpu().numpy(), y_ref, what=f"{which} F={F} gated={gated} {mode} t={t}")
