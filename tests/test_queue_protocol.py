@@ -10,9 +10,15 @@ Protocol (as in the kernel, batch 1, no ordered list requested):
                        the head, reads them in slot order, takes each entry
                        whose tag is this launch's, and stops once every CTA is
                        done and its next slot is at or past the final tail.
+                       A producer claims a batch only while its share table
+                       (own rows included) has room for the whole batch.
 Checked: every active neuron is run exactly once, by its own CTA or through
 the queue; every producer stops; a stale entry from an earlier launch (other
-tag) is never taken."""
+tag) is never taken; with share tables of S rows, no row is lost as long as
+the layer has at most (S - T + 1) neurons per CTA (the bound under which the
+host picks this mode), even when one CTA's range is all active.  A model of
+the earlier claim rule (claim while the table is not full, stop reading a
+claimed batch when it fills) loses rows in the same setting."""
 import random
 
 import pytest
@@ -20,7 +26,7 @@ import pytest
 K_OWN, Q_TAKE = 4, 4
 
 
-def run_protocol(counts, seed, F=None, stale=0):
+def run_protocol(counts, seed, F=None, stale=0, cap=None, old_rule=False):
     rng = random.Random(seed)
     G = len(counts)
     ranges, base = [], 0
@@ -53,27 +59,34 @@ def run_protocol(counts, seed, F=None, stale=0):
         nonlocal head
         while not ready[c]:
             yield
+        held = 0
         for j in own_rows[c]:
             ran.append(j)
+            held += 1
             yield
         pend, pk = -1, 0
         spins = 0
         while True:
             if pend < 0:
+                if cap is not None and (held >= cap if old_rule else held + Q_TAKE > cap):
+                    return                      # table full: this CTA takes no more rows
                 pend, pk = head, 0
                 head += Q_TAKE                  # one atomic add per batch
                 yield
             took = 0
             while pk < Q_TAKE:
+                if cap is not None and old_rule and held >= cap:
+                    break                       # earlier rule: the rest of the batch is never read
                 slot = pend + pk
                 e = qent[slot] if slot < F else None
                 if e is None or e[0] != "now":
                     break
                 ran.append(e[1])
+                held += 1
                 pk += 1
                 took += 1
                 yield
-            if pk == Q_TAKE:
+            if pk == Q_TAKE or (cap is not None and old_rule and held >= cap):
                 pend = -1
                 continue
             if took:
@@ -119,3 +132,34 @@ def test_stale_entries_of_an_earlier_launch_are_never_taken():
     ran, active = run_protocol([6, 9, 0, 12], 3, F=80, stale=80)
     assert sorted(ran) == sorted(active)
     assert -1 not in ran
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_share_table_capacity_keeps_every_row(seed):
+    """Near-dense tokens: every neuron of the widest queue-mode layer active
+    (S - T + 1 neurons per CTA on average, one CTA's range entirely active).
+    With the claim rule of the kernel no row is lost."""
+    S = 16
+    G = 5
+    rng = random.Random(seed)
+    total = (S - Q_TAKE + 1) * G
+    counts = [0] * G
+    for _ in range(total):                      # uneven ranges, one of them large
+        counts[rng.randrange(G) if rng.random() < 0.6 else 0] += 1
+    ran, active = run_protocol(counts, seed, cap=S)
+    assert sorted(ran) == sorted(active)
+
+
+def test_earlier_claim_rule_loses_rows():
+    """The earlier rule, on layers it admitted (up to S neurons per CTA): some
+    interleaving loses a claimed row."""
+    S, G = 16, 5
+    lost = 0
+    for seed in range(40):
+        rng = random.Random(seed)
+        counts = [0] * G
+        for _ in range(S * G - 3):
+            counts[rng.randrange(G) if rng.random() < 0.6 else 0] += 1
+        ran, active = run_protocol(counts, seed, cap=S, old_rule=True)
+        lost += len(active) - len(ran)
+    assert lost > 0
