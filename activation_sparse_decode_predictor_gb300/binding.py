@@ -31,7 +31,7 @@ EXPORTS = ("pi_status_str", "pi_workspace_bytes", "pi_compact_workspace_bytes", 
            "pi_sparse_ffn", "pi_ffn_layer", "pi_dense_ffn", "pi_q4_0_bytes", "pi_quantize_q4_0",
            "pi_quantize_q4_0_host", "pi_fire_counts", "pi_hot_first_perm", "pi_permute_rows", "pi_gather_rows",
            "pi_shard_neurons",
-           "pi_rms_residual", "pi_sync_status", "pi_ffn_layer_static")
+           "pi_rms_residual", "pi_sync_status", "pi_ffn_layer_static", "pi_ffn_layer_chain")
 
 
 class PiError(RuntimeError):
@@ -83,6 +83,7 @@ def lib():
             "pi_rms_residual": ([P, P, i32, i32, P, P], i32),
             "pi_sync_status": ([P, sz, P], i32),
             "pi_ffn_layer_static": ([D, P, P, P, P, P, P, P], i32),
+            "pi_ffn_layer_chain": ([D, P, P, i32, P, P, P, P, P, sz, P], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -248,6 +249,17 @@ def pi_ffn_layer(layer: Layer, x, y, residual=None, idx=None, n_active=None, ws=
         ws = workspace(pi_workspace_bytes(layer, B), x.device)
     _check(lib().pi_ffn_layer(ctypes.byref(layer.desc), _p(x), B, _p(residual), _p(y), _p(idx), _p(n_active),
                               _p(ws), ws.numel(), _stream(stream)), "pi_ffn_layer")
+    return ws
+
+
+def pi_ffn_layer_chain(layer: Layer, x_prev, y_prev, x, y, idx=None, n_active=None, ws=None, stream=None):
+    """Layer of a stack fed by the previous one: x = rms rescale of x_prev +
+    y_prev (written to x), then y = the layer at x."""
+    B_ = x_prev.shape[0] if x_prev.dim() == 2 else 1
+    if ws is None:
+        ws = workspace(pi_workspace_bytes(layer, B_), x_prev.device)
+    _check(lib().pi_ffn_layer_chain(ctypes.byref(layer.desc), _p(x_prev), _p(y_prev), B_, _p(x), _p(y), _p(idx),
+                                    _p(n_active), _p(ws), ws.numel(), _stream(stream)), "pi_ffn_layer_chain")
     return ws
 
 

@@ -325,10 +325,18 @@ pi_status pi_sparse_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, 
     return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s);
 }
 
-pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,
-                       int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes, pi_stream stream)
+}  // extern "C"
+
+namespace {
+
+// pi_ffn_layer, and with x_prev / y_prev given its chained form: the input is
+// then x = (x_prev + y_prev) / rms(x_prev + y_prev), written to x (the one-
+// kernel step computes it in its prologue; other shapes run the glue kernel
+// first).
+pi_status ffn_layer(const pi_ffn_desc *desc, const float *x, const float *x_prev, const float *y_prev, int32_t batch,
+                    const float *residual, float *y, int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes,
+                    cudaStream_t s)
 {
-    Nvtx nv("pi_ffn_layer");
     pi_status st = check_desc(desc, true, true);
     if (st != PI_OK) return st;
     st = check_io(desc, x, batch, residual, y);
@@ -338,7 +346,15 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
     const WsLayout L = ws_layout(desc->d_model, desc->d_ff, desc->rank, batch);
     st = check_ws(ws, ws_bytes, L.total);
     if (st != PI_OK) return st;
-    const cudaStream_t s = (cudaStream_t)stream;
+    const bool chained = x_prev != nullptr;
+    if (chained) {
+        const size_t nb = (size_t)batch * desc->d_model * sizeof(float);
+        if (!y_prev) return PI_ERR_NULL;
+        if (!al(x_prev, 16) || !al(y_prev, 16)) return PI_ERR_ALIGN;
+        if (overlap(x, nb, x_prev, nb) || overlap(x, nb, y_prev, nb) || overlap(y, nb, x_prev, nb) ||
+            overlap(y, nb, y_prev, nb))
+            return PI_ERR_ALIAS;
+    }
     if (batch == 1 && fused_layer_supported(desc->wtype, desc->ptype, desc->d_model, desc->d_ff, desc->rank)) {
         // one kernel per token: predictor, scan and sparse FFN without kernel boundaries
         LayerB1Args a{};
@@ -357,6 +373,9 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
         a.b_act = desc->b_act;
         a.b_down = desc->b_down;
         a.x = x;
+        a.x_prev = chained ? x_prev : nullptr;
+        a.y_prev = chained ? y_prev : nullptr;
+        a.x_out = chained ? const_cast<float *>(x) : nullptr;
         a.residual = residual;
         a.y = y;
         a.idx_out = idx;
@@ -382,6 +401,8 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
         }
         return cuda_status(launch_layer_b1(a, s));
     }
+    if (chained && launch_rms_residual(x_prev, y_prev, batch, desc->d_model, const_cast<float *>(x), s) != cudaSuccess)
+        return PI_ERR_CUDA;
     if (!idx) {
         idx = at<int32_t>(ws, L.idx);
         n_active = at<int32_t>(ws, L.nact);
@@ -391,6 +412,25 @@ pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, c
     // the tensor-core predictor left x's fp16 fragments in the workspace (fp16 layout)
     const bool xf_ready = batch > 1 && desc->ptype == PI_F16 && desc->wtype == PI_F16;
     return enqueue_sparse(desc, x, batch, idx, n_active, y, ws, s, xf_ready);
+}
+
+}  // namespace
+
+extern "C" {
+
+pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,
+                       int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes, pi_stream stream)
+{
+    Nvtx nv("pi_ffn_layer");
+    return ffn_layer(desc, x, nullptr, nullptr, batch, residual, y, idx, n_active, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+pi_status pi_ffn_layer_chain(const pi_ffn_desc *desc, const float *x_prev, const float *y_prev, int32_t batch, float *x,
+                             float *y, int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes, pi_stream stream)
+{
+    Nvtx nv("pi_ffn_layer_chain");
+    if (!x_prev || !y_prev) return PI_ERR_NULL;
+    return ffn_layer(desc, x, x_prev, y_prev, batch, nullptr, y, idx, n_active, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 pi_status pi_dense_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual, float *y,

@@ -139,6 +139,8 @@ struct LayerB1Args {
     const void *w_up, *w_gate, *w_down;
     const float *b_act, *b_down;
     const float *x, *residual;
+    const float *x_prev, *y_prev;  // chained input (x unused): x = (x_prev + y_prev) / rms, written to x_out
+    float *x_out;
     float *y;
     int *idx_out, *n_active;
     int *cand;              // [F] workspace

@@ -80,6 +80,7 @@ struct Tables {
     int count, total;
     unsigned qbase;     // queue mode: the queue slot of the range's k-th active neuron is qbase + k
     int wsum[kNCW];
+    float ssq[kNCW];    // chained input: per-warp sums of squares of x_prev + y_prev
     unsigned words[kMaxRange / 32 + 1];
     unsigned wpre[kMaxRange / 32 + 1];
     float lg[kMaxRange];
@@ -159,6 +160,8 @@ struct FusedParams {
     const uint8_t *w_act, *w_up, *w_down;
     const float *b_act, *b_down;
     const float *x, *residual;
+    const float *x_prev, *y_prev;  // chained input (or null): x = (x_prev + y_prev) / rms(x_prev + y_prev)
+    float *x_out;        // chained input: x is also written here
     float *y;
     int *idx_out;        // ordered active list, or null
     int *n_active;       // or null
@@ -250,9 +253,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 if (qq < nstages) return true;
                 const int s = qq % nstages;
                 const unsigned par = (unsigned)((qq / nstages) - 1) & 1u;
+                if (mbar_try_wait_sleep(&T.empty[s], par, PI_MBAR_SUSPEND_NS)) return true;
                 for (int i = 0; i < (1 << 16); ++i) {
-                    if (mbar_try_wait_sleep(&T.empty[s], par, PI_MBAR_SUSPEND_NS)) return true;
                     if (*fail) return false;
+                    if (mbar_try_wait_sleep(&T.empty[s], par, PI_MBAR_SUSPEND_NS)) return true;
                 }
                 atomicOr(err, ERR_TIMEOUT);
                 return false;
@@ -318,10 +322,6 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             const unsigned par = (unsigned)T.seq & 1u, tag = (unsigned)T.seq + 1u;
             while (!failed) {
                 int kind, i = 0, j = 0;
-                if (*fail) {  // the consumers have stopped: issue nothing more
-                    failed = true;
-                    break;
-                }
                 if (ds < up && state[ds] != 0) {
                     const int stt = state[ds];
                     i = ds++;
@@ -376,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                         pend = -1;
                         continue;
                     }
-                    if (++qspins < plim) {
+                    if (++qspins < plim && !*fail) {  // the consumers have not stopped: wait for entries
                         __nanosleep(32);
                         continue;
                     }
-                    atomicOr(err, ERR_TIMEOUT);
+                    if (!*fail) atomicOr(err, ERR_TIMEOUT);
                     failed = true;
                     kind = kJobEnd;
                 } else if (up < sn) {
@@ -395,9 +395,9 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     kind = kJobUp;
                 } else if (ds < sn) {
                     long long spins = 0;
-                    while (state[ds] == 0 && ++spins < kSpinLimit) __nanosleep(64);
+                    while (state[ds] == 0 && ++spins < kSpinLimit && !*fail) __nanosleep(64);
                     if (state[ds] == 0) {
-                        atomicOr(err, ERR_TIMEOUT);
+                        if (!*fail) atomicOr(err, ERR_TIMEOUT);
                         failed = true;
                         kind = kJobEnd;
                     } else {
@@ -477,18 +477,59 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     }
     float xr[CH][EPC];
     float acc[CH][EPC];
+    const bool chained = p.x_prev != nullptr;
+    const float *xin = chained ? p.x_prev : p.x;
+    float ss = 0.f;
 #pragma unroll
     for (int u = 0; u < CH; ++u) {
         const int cc = t + kNCT * u;
 #pragma unroll
         for (int e = 0; e < EPC; e += 4) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (cc < nch) v = *reinterpret_cast<const float4 *>(p.x + (size_t)cc * EPC + e);
+            if (cc < nch) {
+                v = *reinterpret_cast<const float4 *>(xin + (size_t)cc * EPC + e);
+                if (chained) {
+                    const float4 w = *reinterpret_cast<const float4 *>(p.y_prev + (size_t)cc * EPC + e);
+                    v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+                }
+            }
             xr[u][e] = v.x;
             xr[u][e + 1] = v.y;
             xr[u][e + 2] = v.z;
             xr[u][e + 3] = v.w;
+            if (chained) {
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+            }
             acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
+        }
+    }
+    if (chained) {
+        // the layer-to-layer glue of a stack, done by every CTA for the whole
+        // vector in the same order (so all CTAs hold the same x): v = x_prev +
+        // y_prev, x = v / sqrt(mean(v^2)) (0 when v = 0); this CTA's slice of
+        // x also goes to x_out
+        ss = warp_sum(ss);
+        if (lane == 0) T.ssq[warp] = ss;
+        named_bar_sync(1, kNCT);
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNCW; ++w) tot += T.ssq[w];
+        const float rms = sqrtf(tot / (float)d);
+#pragma unroll
+        for (int u = 0; u < CH; ++u)
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) xr[u][e] = rms > 0.f ? xr[u][e] / rms : 0.f;
+        const int nvec = d / 4;
+        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
+        if (v0 + t < v1) {
+            const float4 a = reinterpret_cast<const float4 *>(p.x_prev)[v0 + t];
+            const float4 b = reinterpret_cast<const float4 *>(p.y_prev)[v0 + t];
+            const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+            reinterpret_cast<float4 *>(p.x_out)[v0 + t] =
+                rms > 0.f ? make_float4(v.x / rms, v.y / rms, v.z / rms, v.w / rms) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     // ok is warp-uniform between CTA barriers (every stage wait is decided for
@@ -920,6 +961,9 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     p.b_down = a.b_down;
     p.x = a.x;
     p.residual = a.residual;
+    p.x_prev = a.x_prev;
+    p.y_prev = a.y_prev;
+    p.x_out = a.x_out;
     p.y = a.y;
     p.idx_out = a.idx_out;
     p.n_active = a.n_active;
@@ -948,7 +992,7 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     sb = (sb + 127u) & ~127u;
     const int need = chunks_per_thread(a.wtype, a.d);
     const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
-    const size_t budget = (size_t)(colocate(epc, need) ? 110 : 200) * 1024;
+    const size_t budget = (size_t)(colocate(epc, need) ? 110 : 216) * 1024;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;

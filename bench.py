@@ -669,11 +669,13 @@ def run_ours(args, w):
 def run_stack(args, w):
     """Workloads of several layers (the OPT-175B-shaped stack): each token goes
     through `w.layers` distinct layers, each layer's output plus its input
-    rescaled by pi_rms_residual into the next layer's input, and the whole token
-    is timed end to end.  Metric: us per layer per token (step time / tokens /
-    layers; the glue kernel is part of it).  The roofline's dominant kernel,
-    k_layer_b1, is also timed alone: the same layer calls back to back on the
-    recorded inputs of every layer."""
+    rescaled into the next layer's input, and the whole token is timed end to
+    end.  Layer 0 runs pi_ffn_layer on the token; every later layer runs
+    pi_ffn_layer_chain, whose kernel applies the glue to the previous layer's
+    input and output itself; one pi_rms_residual finishes the token.  Metric:
+    us per layer per token (step time / tokens / layers).  The roofline's
+    dominant kernel, k_layer_b1, is also timed alone: the same layer calls back
+    to back on the recorded inputs of every layer."""
     world, rank, local = dist_env()
     barrier = None
     if world > 1:
@@ -694,19 +696,25 @@ def run_stack(args, w):
     T, d = X.shape
     ws = B.workspace(B.pi_workspace_bytes(lays[0], 1), X.device)
     ya = torch.empty(d, dtype=torch.float32, device=X.device)
-    bufs = [torch.empty(d, dtype=torch.float32, device=X.device) for _ in range(2)]
+    xs = [torch.empty(d, dtype=torch.float32, device=X.device) for _ in range(2)]
+    ys = [torch.empty(d, dtype=torch.float32, device=X.device) for _ in range(2)]
     Xout = torch.empty(T, d, dtype=torch.float32, device=X.device)
     stream = torch.cuda.Stream()
 
-    def token(xin, xout, record=None):
-        cur = xin
-        for l in range(nl):
-            if record is not None:
-                record[l].copy_(cur)
-            B.pi_ffn_layer(lays[l], cur, ya, ws=ws)
-            nxt = xout if l == nl - 1 else bufs[l % 2]
-            B.pi_rms_residual(cur, ya, nxt)
-            cur = nxt
+    def token(xin, xout, rec_x=None, rec_y=None):
+        B.pi_ffn_layer(lays[0], xin, ys[0], ws=ws)
+        xp, yp = xin, ys[0]
+        if rec_x is not None:
+            rec_x[0].copy_(xin)
+            rec_y[0].copy_(ys[0])
+        for l in range(1, nl):
+            xn, yn = xs[l % 2], ys[l % 2]
+            B.pi_ffn_layer_chain(lays[l], xp, yp, xn, yn, ws=ws)
+            if rec_x is not None:
+                rec_x[l].copy_(xn)
+                rec_y[l].copy_(yn)
+            xp, yp = xn, yn
+        B.pi_rms_residual(xp, yp, xout)
 
     def step(Xin=X):
         for t in range(T):
@@ -714,8 +722,9 @@ def run_stack(args, w):
 
     # statistics on the chained inputs of every layer (outside any timed region)
     Xl = torch.empty(nl, T, d, dtype=torch.float32, device=X.device)
+    Yl = torch.empty(nl, T, d, dtype=torch.float32, device=X.device)
     for t in range(T):
-        token(X[t], Xout[t], record=[Xl[l, t] for l in range(nl)])
+        token(X[t], Xout[t], rec_x=[Xl[l, t] for l in range(nl)], rec_y=[Yl[l, t] for l in range(nl)])
     torch.cuda.synchronize()
     n_pred, n_down, recs, precs, dens, fire = [], [], [], [], [], []
     trues = []
@@ -746,13 +755,16 @@ def run_stack(args, w):
                               "device_status": B.pi_sync_status(ws)}))
         return 0
 
-    # the dominant kernel alone: every layer's k_layer_b1 on its recorded input, back to back
+    # the dominant kernel alone: every layer's k_layer_b1 (as the step calls it) on its
+    # recorded inputs, back to back, without the one glue launch per token
     ksteps = max(4, args.steps // 4)
+    xscratch = torch.empty(d, dtype=torch.float32, device=X.device)
 
     def kernel_only():
         for t in range(T):
-            for l in range(nl):
-                B.pi_ffn_layer(lays[l], Xl[l, t], ya, ws=ws)
+            B.pi_ffn_layer(lays[0], Xl[0, t], ya, ws=ws)
+            for l in range(1, nl):
+                B.pi_ffn_layer_chain(lays[l], Xl[l - 1, t], Yl[l - 1, t], xscratch, ya, ws=ws)
 
     g_k = capture(kernel_only, stream)
     ms_k = time_graph(g_k, ksteps, min(args.warmup, 3), stream) / ksteps
@@ -826,16 +838,17 @@ def run_stack(args, w):
             "roofline": roofline_obj("k_layer_b1 (pi_ffn_layer), timed alone back to back on the stack's inputs",
                                      k_gbs, peak, peak_src, committed_traffic("k_layer_b1", w.name),
                                      launch_us=us_k),
-            "roofline_layer": roofline_obj("stack end to end (k_layer_b1 + glue kernel)", layer_gbs, peak, peak_src,
-                                           None),
+            "roofline_layer": roofline_obj("stack end to end (k_layer_b1, one glue kernel per token)", layer_gbs,
+                                           peak, peak_src, None),
             "kernels": {"per": "layer and token", "layer_kernel_us": us_k, "layer_kernel_gbs": k_gbs,
                         "layer_kernel_frac": k_gbs / peak, "step_us_per_layer": us_tok,
                         "true_mask_sparse_ffn_us": us_tr, "true_mask_sparse_ffn_gbs": tr_b / (us_tr * 1e-6) / 1e9,
                         "true_mask_sparse_ffn_frac": tr_b / (us_tr * 1e-6) / 1e9 / peak,
                         "true_mask_n_mean": float(np.mean(n_true))},
             "e2e": {"value": us_e2e, "unit": "us/layer/token", "h2d_bytes_per_step": int(Xh.numel() * 4),
-                    "d2h_bytes_per_step": int(Yh.numel() * 4), "path": "pi_ffn_layer + pi_rms_residual per layer"},
-            "gpu_launches": 2 * nl * T * args.steps,
+                    "d2h_bytes_per_step": int(Yh.numel() * 4),
+                    "path": "pi_ffn_layer, then pi_ffn_layer_chain per layer, pi_rms_residual per token"},
+            "gpu_launches": (nl + 1) * T * args.steps,
             "clocks": clk.summary(),
             "device_status": st,
         }

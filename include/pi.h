@@ -217,6 +217,28 @@ PI_API pi_status pi_ffn_layer(const pi_ffn_desc *desc, const float *x, int32_t b
                        float *y, int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes,
                        pi_stream stream);
 
+/*
+ * The next layer of a stack whose layers feed each other (one decode token
+ * through consecutive FFN layers): the layer-to-layer glue of pi_rms_residual
+ * and then pi_ffn_layer, fused.  Per token b,
+ *   v = x_prev[b] + y_prev[b],  x[b] = v / sqrt(mean(v^2))  (0 when v = 0),
+ *   y[b] = FFN of this layer at x[b] (no residual),
+ * with x[b] also written out (the next glue step needs it).  For the shapes
+ * where pi_ffn_layer runs one kernel at batch 1, the glue is part of that
+ * kernel: every CTA rescales the whole vector itself, after the previous
+ * layer's kernel has finished, so no launch sits between two layers.  Other
+ * shapes run pi_rms_residual's kernel first.  The stack's input glue follows
+ * the reading of "output plus residual as the next layer's input" taken for
+ * the OPT-175B-shaped stack (weightless RMS rescale of the sum).
+ *   x_prev, y_prev  device fp32 [batch][d_model], 16-byte aligned.
+ *   x, y            device fp32 [batch][d_model]; neither may overlap x_prev
+ *                   or y_prev, and y may not overlap x (PI_ERR_ALIAS).
+ *   idx, n_active, ws, ws_bytes: as in pi_ffn_layer.
+ */
+PI_API pi_status pi_ffn_layer_chain(const pi_ffn_desc *desc, const float *x_prev, const float *y_prev, int32_t batch,
+                                    float *x, float *y, int32_t *idx, int32_t *n_active, void *ws, size_t ws_bytes,
+                                    pi_stream stream);
+
 /* Dense FFN (every neuron), through the same operators; the all-active
  * special case used as a check and as the dense baseline. */
 PI_API pi_status pi_dense_ffn(const pi_ffn_desc *desc, const float *x, int32_t batch, const float *residual,

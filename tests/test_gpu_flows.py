@@ -91,48 +91,102 @@ def test_hot_first_permuted_layer():
     assert np.mean(low) > 0.5
 
 
+def _compare_chain(layers, X0, gpu_x, gpu_sets, what):
+    """Follow the GPU chain with the oracle from the same input: at every layer
+    the GPU's active set must equal the oracle's except at borderline neurons
+    (either decision is correct there; the oracle then takes the GPU's), and
+    the next layer's input must match to the output tolerance."""
+    batch, d = X0.shape
+    xo = X0.astype(np.float32)
+    for l, (_, olay, H) in enumerate(layers):
+        union, amb = _predicted_union(olay, H, xo)
+        ref = set(np.flatnonzero(union).tolist())
+        got = gpu_sets[l]
+        assert all(amb[j] for j in got ^ ref), f"{what} layer {l}: decisions differ away from the threshold"
+        res = np.array(sorted((ref - set(np.flatnonzero(amb))) | (got & set(np.flatnonzero(amb)))), dtype=np.int32)
+        xnext = np.empty((batch, d), dtype=np.float64)
+        for b in range(batch):
+            xnext[b] = oracle.rms_residual(xo[b], oracle.sparse_ffn(olay, xo[b], res))
+            assert_ffn_close(gpu_x[l][b], xnext[b], what=f"{what} layer {l} token {b}")
+        xo = xnext.astype(np.float32)
+
+
+def _run_chain(layers, X0, chained, F):
+    """The stack on the GPU: per layer either pi_ffn_layer then pi_rms_residual,
+    or pi_ffn_layer_chain (glue fused into the next layer), then one final
+    pi_rms_residual.  Returns every layer's output x_{l+1} and active set."""
+    batch, d = X0.shape
+    xs = [_cuda(X0), torch.empty(batch, d, dtype=torch.float32, device="cuda")]
+    ys = [torch.empty(batch, d, dtype=torch.float32, device="cuda") for _ in range(2)]
+    idx = torch.zeros(F, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sq = (lambda t: t) if batch > 1 else (lambda t: t[0])
+    ws = None
+    gpu_x, gpu_sets = [], []
+    for l, (lay, _, _) in enumerate(layers):
+        if not chained:
+            ws = B.pi_ffn_layer(lay, sq(xs[0]), sq(ys[0]), idx=idx, n_active=n, ws=ws)
+            B.pi_rms_residual(xs[0], ys[0], xs[1])
+            xs.reverse()
+        elif l == 0:
+            ws = B.pi_ffn_layer(lay, sq(xs[0]), sq(ys[0]), idx=idx, n_active=n, ws=ws)
+        else:
+            # x_l = glue(x_{l-1}, y_{l-1}) into the other x buffer, y_l into the other y buffer
+            ws = B.pi_ffn_layer_chain(lay, sq(xs[0]), sq(ys[0]), sq(xs[1]), sq(ys[1]), idx=idx, n_active=n, ws=ws)
+            xs.reverse()
+            ys.reverse()
+            gpu_x.append(xs[0].cpu().numpy().copy())   # x_l: the previous layer's output through the glue
+        assert B.pi_sync_status(ws) == 0
+        gpu_sets.append(set(idx.cpu().numpy()[: int(n.item())].tolist()))
+        if not chained:
+            gpu_x.append(xs[0].cpu().numpy().copy())
+    if chained:
+        B.pi_rms_residual(xs[0], ys[0], xs[1])
+        torch.cuda.synchronize()
+        gpu_x.append(xs[1].cpu().numpy().copy())
+    return gpu_x, gpu_sets
+
+
+@pytest.mark.parametrize("chained", [False, True])
 @pytest.mark.parametrize("batch", [1, 4])
-def test_stack_of_twelve_layers(batch):
+def test_stack_of_twelve_layers(batch, chained):
+    """Twelve layers, each output plus residual rescaled into the next layer's
+    input: glue kernel between layers, or fused into the next layer's kernel
+    (pi_ffn_layer_chain)."""
     d, F, r, depth = 512, 2048, 64, 12
     layers = []
     for l in range(depth):
         L = synth.make_layer(d, F, r, gated=False, wtype="f16", sparsity=0.95, seed=900 + l, device="cuda")
         layers.append(make_pair(L))
     X0 = synth.tokens(batch, d, 901).numpy()
+    gpu_x, gpu_sets = _run_chain(layers, X0, chained, F)
+    _compare_chain(layers, X0, gpu_x, gpu_sets, f"batch {batch} chained={chained}")
 
-    # GPU chain: pi_ffn_layer then pi_rms_residual, all on the device
-    xg = _cuda(X0)
-    y = torch.empty(batch, d, dtype=torch.float32, device="cuda")
-    xn = torch.empty(batch, d, dtype=torch.float32, device="cuda")
-    idx = torch.zeros(F, dtype=torch.int32, device="cuda")
-    n = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = None
-    gpu_x, gpu_sets = [], []
-    for lay, _, _ in layers:
-        ws = B.pi_ffn_layer(lay, xg if batch > 1 else xg[0], y if batch > 1 else y[0], idx=idx, n_active=n, ws=ws)
-        B.pi_rms_residual(xg, y, xn)
-        assert B.pi_sync_status(ws) == 0
-        gpu_sets.append(set(idx.cpu().numpy()[: int(n.item())].tolist()))
-        xg, xn = xn, xg
-        gpu_x.append(xg.cpu().numpy().copy())
 
-    # oracle chain from the same input
-    xo = X0.astype(np.float32)
-    for l, (_, olay, H) in enumerate(layers):
-        union, amb = _predicted_union(olay, H, xo)
-        ref = set(np.flatnonzero(union).tolist())
-        diff = gpu_sets[l] ^ ref
-        assert all(amb[j] for j in diff), f"layer {l}: decisions differ away from the threshold"
-        if diff:
-            # a borderline neuron went the other way: both chains are valid from here on
-            break
-        idx_np = np.flatnonzero(union).astype(np.int32)
-        xnext = np.empty((batch, d), dtype=np.float64)
-        for b in range(batch):
-            xnext[b] = oracle.rms_residual(xo[b], oracle.sparse_ffn(olay, xo[b], idx_np))
-        for b in range(batch):
-            assert_ffn_close(gpu_x[l][b], xnext[b], what=f"layer {l} token {b}")
-        xo = xnext.astype(np.float32)
-    else:
-        return
-    pytest.skip(f"chain compared through layer {l - 1}; a borderline decision at layer {l} split the chains")
+def test_chained_glue_matches_separate_glue():
+    """The fused glue and the glue kernel compute the same rescale (sums in a
+    different order): the chains' active sets agree except at borderline
+    neurons and their outputs agree to the output tolerance."""
+    d, F, r, depth = 1024, 4100, 128, 6
+    layers = [make_pair(synth.make_layer(d, F, r, gated=True, wtype="f16", sparsity=0.9, seed=950 + l,
+                                         device="cuda")) for l in range(depth)]
+    X0 = synth.tokens(1, d, 951).numpy()
+    xa, sa = _run_chain(layers, X0, False, F)
+    xb, sb = _run_chain(layers, X0, True, F)
+    for l in range(depth):
+        assert_ffn_close(xb[l][0], xa[l][0].astype(np.float64), what=f"layer {l}")
+        if sa[l] != sb[l]:
+            break  # a borderline neuron split the chains; both stay valid (checked against the oracle elsewhere)
+
+
+@pytest.mark.slow
+def test_opt175b_stack_full_size_chain():
+    """The OPT-175B-shaped stack at full size (12 layers of d_model 12288,
+    d_ff 49152, rank 1024, fp16), the first tokens of the workload through the
+    fused chain the benchmark times, against the oracle chain."""
+    w = synth.WORKLOADS["opt175b-relu-fp16-stack12"]
+    layers = [make_pair(synth.workload_layer(w, l, device="cuda")) for l in range(w.layers)]
+    X = synth.workload_tokens(w, n=2, device="cuda").cpu().numpy()
+    for t in range(X.shape[0]):
+        gpu_x, gpu_sets = _run_chain(layers, X[t:t + 1], True, w.d_ff)
+        _compare_chain(layers, X[t:t + 1], gpu_x, gpu_sets, f"OPT-175B stack token {t}")
