@@ -58,7 +58,8 @@ constexpr int kMaxShare = 512;     // FFN rows per CTA (share of the active list
 constexpr int kMaxRange = 512;     // neurons per CTA range (P2 rows)
 constexpr int kMaxG = 1024;
 constexpr int kMaxRank = 2048;
-constexpr int kGroup = 8;          // P2 rows per job
+constexpr int kGroup = 8;          // P2 rows reduced together (one butterfly)
+constexpr int kMaxRJ = 16;         // P2 rows per job: as many as a stage holds, up to this
 constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
 constexpr int kUpRing = 32;        // FFN up rows in flight (> ring stages)
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     const uint32_t p1row = (uint32_t)d * sizeof(PT), p2row = (uint32_t)r * sizeof(PT);
     const int rp1 = max(1, min(kMaxP1, (int)(stage_bytes / p1row)));  // P1 rows per job
     const int nP1 = (nP1r + rp1 - 1) / rp1;
-    const int nP2 = (nR + kGroup - 1) / kGroup;
+    const int rj = max(1, min(kMaxRJ, (int)(stage_bytes / p2row)));  // P2 rows per job
+    const int nP2 = (nR + rj - 1) / rj;
     // No ordered active list requested (and a layer narrow enough that the
     // CTAs' share tables can hold every neuron, see launch_layer_b1): the FFN
     // rows come from a shared work queue that every CTA feeds with its range's
@@ -262,13 +264,6 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 return false;
             };
             for (int i = 0; i < nP1 + nP2; ++i) {
-                if (i == min(nstages, nP1 + nP2)) {
-                    // the ring is full: ask L2 for the P2 rows still to come, so
-                    // later refills do not wait for HBM (issued after the ring's
-                    // own copies so those are served first)
-                    const int gnext = j0 + max(0, i - nP1) * kGroup;
-                    if (gnext < j1) prefetch_l2(p.p2 + (size_t)gnext * p2row, (uint32_t)(j1 - gnext) * p2row);
-                }
                 if (!acquire(q)) {
                     failed = true;
                     break;
@@ -280,13 +275,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     const uint32_t bytes = (uint32_t)(k1 - k0) * p1row;
                     T.job[s] = make_int4(kJobP1, k0, k1, 0);
                     mbar_arrive_expect_tx(&T.full[s], bytes);
-                    bulk_g2s(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s]);
+                    bulk_g2s_once(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s]);
                 } else {
-                    const int g0 = j0 + (i - nP1) * kGroup, g1 = min(g0 + kGroup, j1);
+                    const int g0 = j0 + (i - nP1) * rj, g1 = min(g0 + rj, j1);
                     const uint32_t bytes = (uint32_t)(g1 - g0) * p2row;
                     T.job[s] = make_int4(kJobP2, g0, g1, 0);
                     mbar_arrive_expect_tx(&T.full[s], bytes);
-                    bulk_g2s(st, p.p2 + (size_t)g0 * p2row, bytes, &T.full[s]);
+                    bulk_g2s_once(st, p.p2 + (size_t)g0 * p2row, bytes, &T.full[s]);
                 }
                 ++q;
             }
@@ -617,8 +612,9 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         for (int e = 0; e < PEPC; ++e) hreg[u][e] = (lane + 32 * u < nc2) ? T.hs[(lane + 32 * u) * PEPC + e] : 0.f;
 
     // ---- 2. logits of this CTA's neuron range: each warp takes whole P2 jobs
-    //         (up to 8 rows) round-robin, keeps all rows in flight, and reduces
-    //         the rows together with one transposed butterfly (9 shuffles) ----
+    //         (a full stage, up to 16 rows) round-robin and works through a job
+    //         8 rows at a time, keeping those rows in flight and reducing them
+    //         together with one transposed butterfly (9 shuffles) ----
     {
         static_assert(kGroup == 8, "butterfly below reduces 8 rows");
         // Rounds of m <= #stages jobs, one per warp, with a consumer barrier
@@ -641,45 +637,50 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             const uint8_t *st = stages + (size_t)s * stage_bytes;
             const int4 job = T.job[s];
             const int nrow = job.z - job.y;
-            // All 8 rows, branch-free, so their loads and FMA chains
-            // interleave: rows past nrow read stage bytes that are in bounds
-            // and are discarded; chunks past the row end load zeros.
-            float v[kGroup];
+            for (int h0 = 0; h0 < nrow; h0 += kGroup) {  // warp-uniform
+                const uint8_t *sh = st + (size_t)h0 * p2row;
+                const int nh = min(kGroup, nrow - h0);
+                // All 8 rows, branch-free apart from rows past the job's end
+                // (not read, so no read leaves the stage), so their loads and FMA
+                // chains interleave; chunks past the row end load zeros.
+                float v[kGroup];
 #pragma unroll
-            for (int rr = 0; rr < kGroup; ++rr) v[rr] = 0.f;
+                for (int rr = 0; rr < kGroup; ++rr) v[rr] = 0.f;
 #pragma unroll
-            for (int u = 0; u < kHreg; ++u) {
-                const bool in = lane + 32 * u < nc2;
+                for (int u = 0; u < kHreg; ++u) {
+                    const bool in = lane + 32 * u < nc2;
 #pragma unroll
-                for (int rr = 0; rr < kGroup; ++rr) {
-                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                    if (in) w = *reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)(lane + 32 * u) * 16);
-                    v[rr] += dot16<PT>(w, hreg[u]);
+                    for (int rr = 0; rr < kGroup; ++rr) {
+                        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                        if (in && rr < nh) w = *reinterpret_cast<const uint4 *>(sh + (size_t)rr * p2row + (size_t)(lane + 32 * u) * 16);
+                        v[rr] += dot16<PT>(w, hreg[u]);
+                    }
                 }
-            }
-            for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {  // ranks above 32*kHreg*PEPC
+                for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {  // ranks above 32*kHreg*PEPC
 #pragma unroll
-                for (int rr = 0; rr < kGroup; ++rr)
-                    v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)cc * 16),
-                                       &T.hs[cc * PEPC]);
-            }
-            // lanes exchange halves of their row set: after the three steps
-            // lane l holds row 4*b4 + 2*b3 + b2 (bits of l) summed over the 8
-            // lanes sharing those bits; two more steps finish the sum
-#pragma unroll
-            for (int m = 16, n = kGroup / 2; m >= 4; m >>= 1, n >>= 1) {
-                const bool upper = (lane & m) != 0;
-#pragma unroll
-                for (int k = 0; k < n; ++k) {
-                    const float send = upper ? v[k] : v[k + n];
-                    const float keep = upper ? v[k + n] : v[k];
-                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    for (int rr = 0; rr < kGroup; ++rr)
+                        if (rr < nh)
+                            v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(sh + (size_t)rr * p2row + (size_t)cc * 16),
+                                               &T.hs[cc * PEPC]);
                 }
+                // lanes exchange halves of their row set: after the three steps
+                // lane l holds row 4*b4 + 2*b3 + b2 (bits of l) summed over the 8
+                // lanes sharing those bits; two more steps finish the sum
+#pragma unroll
+                for (int m = 16, n = kGroup / 2; m >= 4; m >>= 1, n >>= 1) {
+                    const bool upper = (lane & m) != 0;
+#pragma unroll
+                    for (int k = 0; k < n; ++k) {
+                        const float send = upper ? v[k] : v[k + n];
+                        const float keep = upper ? v[k + n] : v[k];
+                        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    }
+                }
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+                const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                if ((lane & 3) == 0 && rr < nh) T.lg[job.y + h0 + rr - j0] = v[0] + T.pb[job.y + h0 + rr - j0];
             }
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-            const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-            if ((lane & 3) == 0 && rr < nrow) T.lg[job.y + rr - j0] = v[0] + T.pb[job.y + rr - j0];
             // the stage's empty barrier counts one arrival per consumer warp:
             // this warp consumed it alone, so it arrives for all of them
             __syncwarp();
@@ -988,11 +989,40 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     }
     const int esz = a.ptype == 1 ? 2 : 4;
     const uint32_t R = row_slot_bytes(a.wtype, a.d);
-    uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
-    sb = (sb + 127u) & ~127u;
     const int need = chunks_per_thread(a.wtype, a.d);
     const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
     const size_t budget = (size_t)(colocate(epc, need) ? 110 : 216) * 1024;
+    // Stage size: a P1 row, the FFN rows of one neuron, and a P2 job of at
+    // least 8 rows.  Larger P2 jobs (up to 16 rows, a full stage) are taken
+    // when they cut the logits phase's rounds (one job per consumer warp per
+    // round) without leaving the ring fewer than 9 stages (or its size with
+    // 8-row jobs, when that is already smaller).
+    const uint32_t p2b = (uint32_t)a.r * esz;
+    const uint32_t base = std::max<uint32_t>((uint32_t)a.d * esz, (a.gated ? 2u : 1u) * R);
+    auto stages_of = [&](uint32_t b) {
+        b = (b + 127u) & ~127u;
+        return (int)std::min<size_t>(kMaxStages, (budget - kHdr) / b);
+    };
+    uint32_t sb = std::max<uint32_t>(base, (uint32_t)kGroup * p2b);
+    {
+        const int floor_ns = std::min(stages_of(sb), 9);
+        const int nr = (a.F + G - 1) / G;
+        int best = 1 << 30;
+        uint32_t pick = sb;
+        for (int rjc = kGroup; rjc <= kMaxRJ; ++rjc) {
+            const uint32_t b = std::max<uint32_t>(base, (uint32_t)rjc * p2b);
+            const int nsc = stages_of(b);
+            if (nsc < floor_ns || nsc < 2) continue;
+            const int jobs = (nr + rjc - 1) / rjc, mr = std::min(kNCW, nsc);
+            const int rounds = (jobs + mr - 1) / mr;
+            if (rounds < best) {
+                best = rounds;
+                pick = b;
+            }
+        }
+        sb = pick;
+    }
+    sb = (sb + 127u) & ~127u;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
