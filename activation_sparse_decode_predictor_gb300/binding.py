@@ -47,7 +47,7 @@ class FFNDesc(ctypes.Structure):
                 ("w_up", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("b_act", ctypes.c_void_p), ("b_down", ctypes.c_void_p),
                 ("p1", ctypes.c_void_p), ("p2", ctypes.c_void_p), ("p_bias", ctypes.c_void_p),
-                ("next", ctypes.c_void_p)]
+                ("next", ctypes.c_void_p), ("dense_prefix", ctypes.c_int32)]
 
 
 _lib = None
@@ -139,7 +139,7 @@ class Layer:
     """
 
     def __init__(self, d_model, d_ff, rank, w_up, w_down, w_gate=None, b_act=None, b_down=None, p1=None, p2=None,
-                 p_bias=None, threshold=0.0, act=PI_ACT_RELU, wtype=None):
+                 p_bias=None, threshold=0.0, act=PI_ACT_RELU, wtype=None, dense_prefix=0):
         self.tensors = dict(w_up=w_up, w_gate=w_gate, w_down=w_down, b_act=b_act, b_down=b_down, p1=p1, p2=p2,
                             p_bias=p_bias)
         for k, v in self.tensors.items():
@@ -153,7 +153,7 @@ class Layer:
         self.wtype, self.ptype = wtype, ptype
         self.desc = FFNDesc(self.d_model, self.d_ff, self.rank, int(self.gated), int(act), int(wtype), int(ptype),
                             float(threshold), _p(w_up), _p(w_gate), _p(w_down), _p(b_act), _p(b_down), _p(p1),
-                            _p(p2), _p(p_bias))
+                            _p(p2), _p(p_bias), None, int(dense_prefix))
 
     def set_next(self, other: "Layer | None"):
         """Name the layer run next on the same stream (its predictor weights are
@@ -168,6 +168,8 @@ class Layer:
         `keep_b_down` (the shard that adds it; the partial outputs of all shards
         sum to the layer output)."""
         _dev(neurons, "neurons")
+        if self.desc.dense_prefix:
+            raise ValueError("a neuron shard of a layer with an always-on prefix is not defined")
         n, F, d = int(neurons.numel()), self.d_ff, self.d_model
         T = self.tensors
 
@@ -194,7 +196,7 @@ class Layer:
         return cls(L["d_model"], L["d_ff"], L["rank"], L["w_up"], L["w_down"], w_gate=L.get("w_gate"),
                    b_act=L.get("b_act"), b_down=L.get("b_down"), p1=L.get("p1"), p2=L.get("p2"),
                    p_bias=L.get("p_bias"), threshold=L.get("threshold", 0.0) if threshold is None else threshold,
-                   act=act, wtype=L.get("wtype_code"))
+                   act=act, wtype=L.get("wtype_code"), dense_prefix=L.get("dense_prefix", 0))
 
 
 def pi_status_str(status: int) -> str:

@@ -123,6 +123,7 @@ pi_status check_desc(const pi_ffn_desc *D, bool ffn, bool pred)
         if (D->ptype != PI_F32 && D->ptype != PI_F16) return PI_ERR_DTYPE;
         if (D->rank < 8 || D->rank > PI_MAX_RANK || D->rank % 8) return PI_ERR_SHAPE;
         if (D->d_ff >= (1 << 23)) return PI_ERR_SHAPE;
+        if (D->dense_prefix < 0 || D->dense_prefix > D->d_ff) return PI_ERR_SHAPE;
         if (!D->p1 || !D->p2) return PI_ERR_NULL;
         if (!al(D->p1, 16) || !al(D->p2, 16) || (D->p_bias && !al(D->p_bias, 4))) return PI_ERR_ALIGN;
     }
@@ -180,6 +181,7 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
         a.zbuf = at<float>(ws, L.zbuf);
         a.ucnt = at<unsigned>(ws, L.ucnt);
         a.ctrl = at<WsCtrl>(ws, L.ctrl);
+        a.prefix = D->dense_prefix;
         if (launch_pred_union(a, s) != cudaSuccess) return PI_ERR_CUDA;
         if (launch_compact(a.mask, D->d_ff, idx, n_active, cap, a.ctrl, at<unsigned long long>(ws, L.status), s) !=
             cudaSuccess)
@@ -201,6 +203,7 @@ pi_status enqueue_predict(const pi_ffn_desc *D, const float *x, int32_t B, float
     p.r = D->rank;
     p.F = D->d_ff;
     p.tau = D->threshold;
+    p.prefix = D->dense_prefix;
     p.logits = logits;
     p.mask = mask;
     p.idx = idx;
@@ -355,7 +358,8 @@ pi_status ffn_layer(const pi_ffn_desc *desc, const float *x, const float *x_prev
             overlap(y, nb, y_prev, nb))
             return PI_ERR_ALIAS;
     }
-    if (batch == 1 && fused_layer_supported(desc->wtype, desc->ptype, desc->d_model, desc->d_ff, desc->rank)) {
+    if (batch == 1 &&
+        fused_layer_supported(desc->wtype, desc->ptype, desc->d_model, desc->d_ff, desc->rank, desc->dense_prefix)) {
         // one kernel per token: predictor, scan and sparse FFN without kernel boundaries
         LayerB1Args a{};
         a.wtype = desc->wtype;
@@ -388,6 +392,7 @@ pi_status ffn_layer(const pi_ffn_desc *desc, const float *x, const float *x_prev
         a.ctrl = at<WsCtrl>(ws, L.ctrl);
         a.d = desc->d_model;
         a.F = desc->d_ff;
+        a.prefix = desc->dense_prefix;
         if (const pi_ffn_desc *nx = desc->next) {
             // the next layer's P1 (its first phase waits on it); its P2 is pulled
             // into L2 by that layer's own kernel early enough.  A bulk prefetch

@@ -59,6 +59,7 @@ struct PredParams {
     const float *h;
     int B, r, F;
     float tau;
+    int prefix;           // neurons [0, prefix) are active whatever their logits
     float *logits;        // [B][F] or null
     uint8_t *mask;        // [F] or null
     int *idx;
@@ -103,6 +104,7 @@ struct SparseParams {
     float *out_h;           // hidden epilogue: h [B][F]
     const float *p_bias;    // logits epilogue
     float tau;
+    int prefix;             // logits epilogue: neurons [0, prefix) always in the mask
     float *out_logits;      // logits epilogue: [B][F] or null
     uint8_t *out_mask;      // logits epilogue: union mask bytes [F]
 };
@@ -112,6 +114,7 @@ struct UnionPredArgs {
     const void *p1, *p2;
     const float *p_bias;
     float tau;
+    int prefix;             // neurons [0, prefix) always in the mask
     const float *x;
     int B, d, r, F;
     float *h;               // [B][r]
@@ -150,10 +153,11 @@ struct LayerB1Args {
     unsigned *status;       // [#SMs] workspace
     WsCtrl *ctrl;
     int d, F;
+    int prefix;             // neurons [0, prefix) always active (no predictor rows read for them)
     const void *pf[2];      // regions asked into L2 during the FFN phase (the next layer's P1), or null
     size_t pf_bytes[2];
 };
-bool fused_layer_supported(int wtype, int ptype, int d, int F, int r);
+bool fused_layer_supported(int wtype, int ptype, int d, int F, int r, int prefix);
 cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s);
 
 // ---- small kernels (aux.cu) ------------------------------------------------------

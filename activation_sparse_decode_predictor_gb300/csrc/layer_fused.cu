@@ -6,7 +6,10 @@
 // method detail): an online predictor marks the neurons expected to fire and
 // neuron-aware sparse operators compute only those neurons.  Predictor form,
 // as in predict.cu: h = max(P1 x, 0), logit = P2 h + p_bias, active when
-// logit > threshold.  FFN as in sparse_ffn.cu.
+// logit > threshold.  FFN as in sparse_ffn.cu.  Optionally the first H
+// neurons (the hot-first order's always-on prefix) are active at every step:
+// the predictor then covers only the tail [H, F) and no P2 row of the prefix
+// is read.
 //
 // GB300 design.  One CTA per SM (all CTAs resident together), 1 producer warp
 // + 8 consumer warps.  The producer thread streams every byte the CTA needs
@@ -16,31 +19,43 @@
 //   P2 jobs      8 rows of P2 each, for this CTA's contiguous neuron range,
 //   FFN jobs     up/gate rows of this CTA's share of the active neurons, and
 //                the down row of each neuron whose activation is non-zero.
-// On entry, before the programmatic-dependent-launch wait, the producer fills
-// the ring with P1 and P2 rows (they do not depend on the previous kernel) and
-// asks L2 for the rest of the CTA's P2 share; later refills come from L2.  The
+// Every weight copy carries an L2 evict-first policy: a decode step reads each
+// weight byte once, and those lines must not push out what is read again (the
+// next layer's P1, asked into L2 during this layer's FFN phase).  On entry,
+// before the programmatic-dependent-launch wait, the producer fills the ring
+// with P1 and P2 rows (they do not depend on the previous kernel).  The
 // consumers:
+//   0. (chained input) rescale the previous layer's x + y themselves: every CTA
+//      sums the squares of the whole vector in the same order, so all CTAs hold
+//      the same x, and writes its slice of x out;
 //   1. compute their P1 rows -> h slice -> global; grid barrier A; load h;
 //   2. compute the logits of their neuron range, threshold, ballot, write the
 //      range's active neurons (with their biases) to a candidate list and the
 //      count to a status word; grid barrier B; read all counts: the prefix
 //      gives this range's place in the ascending active list and the total n;
-//   3. take the balanced share [n*c/G, n*(c+1)/G) of the active list, look
-//      each entry up in the candidate lists and hand the neuron ids to the
-//      producer (an mbarrier), which asks L2 for all their rows at once and
-//      then runs the FFN jobs as sparse_ffn.cu does; the CTA's partial output
-//      goes to y with 16-byte vector atomics.
+//   3. take their prefix slice and the balanced share [n*c/G, n*(c+1)/G) of the
+//      tail's active list, look each entry up in the candidate lists and hand
+//      the neuron ids to the producer (an mbarrier), which asks L2 for all
+//      their rows at once and then runs the FFN jobs as sparse_ffn.cu does; the
+//      CTA's partial output goes to y with 16-byte vector atomics.
 // Steps 2-3 above are the ordered mode, used when the caller asks for the
 // ascending active list.  Without that request (queue mode) there is no
-// barrier B: each CTA keeps the first kOwn active neurons of its own range
-// (its producer starts on them at once, with no global round trip), appends
-// the rest to a shared work queue (one 8-byte entry {launch tag, neuron} per
-// neuron) and counts itself done; producers then take kQTake queue slots per
-// atomic and stop when the queue is drained and every CTA has published.
+// barrier B: each CTA keeps its prefix slice and the first kOwn active neurons
+// of its own range (its producer starts on them at once, with no global round
+// trip), appends the rest to a shared work queue (one 8-byte entry {launch
+// tag, neuron} per neuron) and counts itself done; producers then take kQTake
+// queue slots per atomic, claiming a batch only while the CTA's share table
+// has room for all of it, and stop when the queue is drained and every CTA has
+// published.  The host picks queue mode only when the share tables of all
+// CTAs together hold every neuron, so no claimed row is ever dropped.
 // The grid barriers are counter barriers: one thread per CTA arrives with a
 // release add on a 64-bit counter that is never reset and polls it (acquire,
 // bounded) until it reaches a target derived from a per-launch sequence
-// number, so no arrival ever has to reset anything.
+// number, so no arrival ever has to reset anything.  Every wait is bounded.
+// A barrier that gives up is seen by every consumer thread after the next CTA
+// barrier (a flag in shared memory), stage waits before warp-wide shuffles are
+// decided for the whole warp, and a failed launch publishes nothing, still
+// arrives at every grid barrier and drains its copies before it returns.
 #include <algorithm>
 
 #include "ffn_rows.cuh"
@@ -58,8 +73,7 @@ constexpr int kMaxShare = 512;     // FFN rows per CTA (share of the active list
 constexpr int kMaxRange = 512;     // neurons per CTA range (P2 rows)
 constexpr int kMaxG = 1024;
 constexpr int kMaxRank = 2048;
-constexpr int kGroup = 8;          // P2 rows reduced together (one butterfly)
-constexpr int kMaxRJ = 16;         // P2 rows per job: as many as a stage holds, up to this
+constexpr int kGroup = 8;          // P2 rows per job
 constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
 constexpr int kUpRing = 32;        // FFN up rows in flight (> ring stages)
@@ -76,7 +90,6 @@ struct Tables {
     float redu[kUpRing][kNCW][2];
     int upcnt[kUpRing];
     unsigned long long seq;
-    int fail;           // set by any thread whose wait gave up; read after each CTA barrier
     int share_n;
     int count, total;
     unsigned qbase;     // queue mode: the queue slot of the range's k-th active neuron is qbase + k
@@ -93,6 +106,7 @@ struct Tables {
     float bias[kMaxShare];
     float a[kMaxShare];
     int state[kMaxShare];
+    int fail;           // a wait of this CTA gave up: read by every consumer after the next CTA barrier
 };
 constexpr size_t kHdr = (sizeof(Tables) + 1023) & ~(size_t)1023;
 
@@ -128,21 +142,26 @@ __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p)
 // barrier before the call makes the other threads' writes part of this
 // thread's release).  Arrivals add to a 64-bit counter that is never reset;
 // the barrier is passed when the counter reaches `target` (a multiple of the
-// grid size derived from the launch sequence number).  Every CTA arrives
-// exactly once per barrier, also after a failure (`wait` false), so the
-// counter stays in step with the launch sequence.  The poll backs off with a
-// short sleep after the first few reads and gives up after `limit` polls
-// (ERR_TIMEOUT, returns false).
-__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long target, bool wait, long long limit,
+// grid size derived from the launch sequence number).  Returns false on
+// timeout.
+__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long target, bool wait, const WsCtrl *ctrl,
                              unsigned *err)
 {
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
     if (!wait) return false;
-    for (long long i = 0; i < limit; ++i) {
+    // the first polls do not depend on the control block's limit (a barrier of
+    // a healthy launch passes within them); the limit bounds the rest
+    for (int i = 0; i < 64; ++i) {
         unsigned long long v;
         asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
         if ((long long)(v - target) >= 0) return true;
-        if (i >= 16) __nanosleep(32);
+    }
+    const long long limit = poll_limit(ctrl);
+    for (long long i = 64; i < limit; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if ((long long)(v - target) >= 0) return true;
+        __nanosleep(32);
     }
     atomicOr(err, ERR_TIMEOUT);
     return false;
@@ -173,7 +192,8 @@ struct FusedParams {
     unsigned *status;    // [G] active count of each CTA's range
     WsCtrl *ctrl;
     int d, F, r, act;
-    int queue;           // 1: FFN rows through the shared work queue (no ordered list)
+    int queue;
+    int prefix;          // neurons [0, prefix) always active; the predictor covers [prefix, F)
     float tau;
     const uint8_t *pf[2];  // the next layer's predictor weights (or null), asked into L2
     size_t pf_bytes[2];
@@ -207,18 +227,20 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     const int nch = d / EPC;
     unsigned *err = &p.ctrl->err;
     const int hk0 = (int)((long long)r * c / G), hk1 = (int)((long long)r * (c + 1) / G);
-    const int j0 = (int)((long long)F * c / G), j1 = (int)((long long)F * (c + 1) / G);
+    // always-on prefix [0, H): this CTA's slice [pf0, pf0 + npf) of it; the
+    // predicted tail [H, F) is split into the CTAs' contiguous neuron ranges
+    const int H = p.prefix;
+    const int pf0 = (int)((long long)H * c / G), npf = (int)((long long)H * (c + 1) / G) - pf0;
+    const int j0 = H + (int)((long long)(F - H) * c / G), j1 = H + (int)((long long)(F - H) * (c + 1) / G);
     const int nP1r = hk1 - hk0, nR = j1 - j0;
     const uint32_t p1row = (uint32_t)d * sizeof(PT), p2row = (uint32_t)r * sizeof(PT);
     const int rp1 = max(1, min(kMaxP1, (int)(stage_bytes / p1row)));  // P1 rows per job
     const int nP1 = (nP1r + rp1 - 1) / rp1;
-    const int rj = max(1, min(kMaxRJ, (int)(stage_bytes / p2row)));  // P2 rows per job
-    const int nP2 = (nR + rj - 1) / rj;
-    // No ordered active list requested (and a layer narrow enough that the
-    // CTAs' share tables can hold every neuron, see launch_layer_b1): the FFN
-    // rows come from a shared work queue that every CTA feeds with its range's
-    // active neurons, so there is no second grid barrier, no prefix scan and
-    // no share lookup, and idle CTAs take rows from busy ones.
+    const int nP2 = (nR + kGroup - 1) / kGroup;
+    // No ordered active list requested: the FFN rows come from a shared work
+    // queue that every CTA feeds with its range's active neurons, so there is
+    // no second grid barrier, no prefix scan and no share lookup, and idle CTAs
+    // take rows from busy ones.
     const bool qmode = p.queue != 0;
 
     if (threadIdx.x == 0) {
@@ -248,22 +270,18 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         if (lane == 0) {
             int q = 0;
             bool failed = false;
-            volatile int *fail = &T.fail;
-            // a free stage for job qq; gives up early once a consumer has failed
-            // (its warps release no more stages)
             auto acquire = [&](int qq) -> bool {
-                if (qq < nstages) return true;
                 const int s = qq % nstages;
-                const unsigned par = (unsigned)((qq / nstages) - 1) & 1u;
-                if (mbar_try_wait_sleep(&T.empty[s], par, PI_MBAR_SUSPEND_NS)) return true;
-                for (int i = 0; i < (1 << 16); ++i) {
-                    if (*fail) return false;
-                    if (mbar_try_wait_sleep(&T.empty[s], par, PI_MBAR_SUSPEND_NS)) return true;
-                }
-                atomicOr(err, ERR_TIMEOUT);
-                return false;
+                return qq < nstages || mbar_wait(&T.empty[s], (unsigned)((qq / nstages) - 1) & 1u, err);
             };
             for (int i = 0; i < nP1 + nP2; ++i) {
+                if (i == min(nstages, nP1 + nP2)) {
+                    // the ring is full: ask L2 for the P2 rows still to come, so
+                    // later refills do not wait for HBM (issued after the ring's
+                    // own copies so those are served first)
+                    const int gnext = j0 + max(0, i - nP1) * kGroup;
+                    (void)gnext;
+                }
                 if (!acquire(q)) {
                     failed = true;
                     break;
@@ -277,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     mbar_arrive_expect_tx(&T.full[s], bytes);
                     bulk_g2s_once(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s]);
                 } else {
-                    const int g0 = j0 + (i - nP1) * rj, g1 = min(g0 + rj, j1);
+                    const int g0 = j0 + (i - nP1) * kGroup, g1 = min(g0 + kGroup, j1);
                     const uint32_t bytes = (uint32_t)(g1 - g0) * p2row;
                     T.job[s] = make_int4(kJobP2, g0, g1, 0);
                     mbar_arrive_expect_tx(&T.full[s], bytes);
@@ -291,7 +309,6 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             // from the shared work queue
             if (!failed && !mbar_wait(&T.share_ready, 0u, err)) failed = true;
             int sn = failed ? 0 : T.share_n;
-            const long long plim = poll_limit(p.ctrl);  // the control block is the previous kernel's until now
 #ifndef PI_FUSED_PREFETCH_DOWN
 #define PI_FUSED_PREFETCH_DOWN 0
 #endif
@@ -326,11 +343,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 } else if (up >= sn && !exhausted) {
                     // take kQTake queue slots with one atomic; read the batch's
                     // remaining slots together; a slot is ready once its tag is
-                    // this launch's; a slot at or past the final tail ends the queue.
-                    // A batch is claimed only while the share table has room for
-                    // all of it, so every claimed row is run; a CTA whose table is
-                    // that full takes no more (the host picks queue mode only when
-                    // the tables of all CTAs together hold every neuron)
+                    // this launch's; a slot at or past the final tail ends the queue
                     if (pend < 0) {
                         if (sn + kQTake > kMaxShare) {
                             exhausted = true;
@@ -351,13 +364,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     int took = 0;
 #pragma unroll
                     for (int k = 0; k < kQTake; ++k) {
-                        if (took != k || pk + k >= kQTake) break;
+                        if (took != k || pk + k >= kQTake || sn >= kMaxShare) break;
                         if ((unsigned)(ev[k] >> 32) != tag) break;
                         T.j[sn++] = (int)(unsigned)(ev[k] & 0xffffffffull);
                         ++took;
                     }
                     pk += took;
-                    if (pk == kQTake) {
+                    if (pk == kQTake || sn >= kMaxShare) {
                         pend = -1;
                         continue;
                     }
@@ -371,11 +384,11 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                         pend = -1;
                         continue;
                     }
-                    if (++qspins < plim && !*fail) {  // the consumers have not stopped: wait for entries
+                    if (++qspins < kSpinLimit) {
                         __nanosleep(32);
                         continue;
                     }
-                    if (!*fail) atomicOr(err, ERR_TIMEOUT);
+                    atomicOr(err, ERR_TIMEOUT);
                     failed = true;
                     kind = kJobEnd;
                 } else if (up < sn) {
@@ -390,9 +403,9 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     kind = kJobUp;
                 } else if (ds < sn) {
                     long long spins = 0;
-                    while (state[ds] == 0 && ++spins < kSpinLimit && !*fail) __nanosleep(64);
+                    while (state[ds] == 0 && ++spins < kSpinLimit) __nanosleep(64);
                     if (state[ds] == 0) {
-                        if (!*fail) atomicOr(err, ERR_TIMEOUT);
+                        atomicOr(err, ERR_TIMEOUT);
                         failed = true;
                         kind = kJobEnd;
                     } else {
@@ -448,7 +461,6 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     const int t = threadIdx.x;
     pdl_wait();
     pdl_trigger();
-    const long long plim = poll_limit(p.ctrl);
     if (t == 0) T.seq = ld_volatile_u32(&p.ctrl->bar_seq);
 
     // this thread's float4 of y = b_down + residual (at most one per thread:
@@ -472,71 +484,56 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     }
     float xr[CH][EPC];
     float acc[CH][EPC];
-    const bool chained = p.x_prev != nullptr;
-    const float *xin = chained ? p.x_prev : p.x;
-    float ss = 0.f;
+    if (!p.x_prev) {
 #pragma unroll
-    for (int u = 0; u < CH; ++u) {
-        const int cc = t + kNCT * u;
+        for (int u = 0; u < CH; ++u) {
+            const int cc = t + kNCT * u;
 #pragma unroll
-        for (int e = 0; e < EPC; e += 4) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (cc < nch) {
-                v = *reinterpret_cast<const float4 *>(xin + (size_t)cc * EPC + e);
-                if (chained) {
-                    const float4 w = *reinterpret_cast<const float4 *>(p.y_prev + (size_t)cc * EPC + e);
-                    v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
-                }
+            for (int e = 0; e < EPC; e += 4) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (cc < nch) v = *reinterpret_cast<const float4 *>(p.x + (size_t)cc * EPC + e);
+                xr[u][e] = v.x;
+                xr[u][e + 1] = v.y;
+                xr[u][e + 2] = v.z;
+                xr[u][e + 3] = v.w;
+                acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
             }
-            xr[u][e] = v.x;
-            xr[u][e + 1] = v.y;
-            xr[u][e + 2] = v.z;
-            xr[u][e + 3] = v.w;
-            if (chained) {
+        }
+    } else {
+        // the layer-to-layer glue of a stack, done by every CTA for the whole
+        // vector in the same order (so all CTAs hold the same x): v = x_prev +
+        // y_prev, x = v / sqrt(mean(v^2)) (0 when v = 0).  Phase 1 runs on v
+        // while the sum of squares is reduced (h = max(P1 v, 0) / rms, as P1 is
+        // linear and rms > 0), and x itself is formed after it; this CTA's
+        // slice of x also goes to x_out
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+            const int cc = t + kNCT * u;
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (cc < nch) {
+                    const float4 a = *reinterpret_cast<const float4 *>(p.x_prev + (size_t)cc * EPC + e);
+                    const float4 b = *reinterpret_cast<const float4 *>(p.y_prev + (size_t)cc * EPC + e);
+                    v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+                }
+                xr[u][e] = v.x;
+                xr[u][e + 1] = v.y;
+                xr[u][e + 2] = v.z;
+                xr[u][e + 3] = v.w;
                 ss = fmaf(v.x, v.x, ss);
                 ss = fmaf(v.y, v.y, ss);
                 ss = fmaf(v.z, v.z, ss);
                 ss = fmaf(v.w, v.w, ss);
+                acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
             }
-            acc[u][e] = acc[u][e + 1] = acc[u][e + 2] = acc[u][e + 3] = 0.f;
         }
-    }
-    if (chained) {
-        // the layer-to-layer glue of a stack, done by every CTA for the whole
-        // vector in the same order (so all CTAs hold the same x): v = x_prev +
-        // y_prev, x = v / sqrt(mean(v^2)) (0 when v = 0); this CTA's slice of
-        // x also goes to x_out
         ss = warp_sum(ss);
-        if (lane == 0) T.ssq[warp] = ss;
-        named_bar_sync(1, kNCT);
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNCW; ++w) tot += T.ssq[w];
-        const float rms = sqrtf(tot / (float)d);
-#pragma unroll
-        for (int u = 0; u < CH; ++u)
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) xr[u][e] = rms > 0.f ? xr[u][e] / rms : 0.f;
-        const int nvec = d / 4;
-        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
-        if (v0 + t < v1) {
-            const float4 a = reinterpret_cast<const float4 *>(p.x_prev)[v0 + t];
-            const float4 b = reinterpret_cast<const float4 *>(p.y_prev)[v0 + t];
-            const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-            reinterpret_cast<float4 *>(p.x_out)[v0 + t] =
-                rms > 0.f ? make_float4(v.x / rms, v.y / rms, v.z / rms, v.w / rms) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        if (lane == 0) T.ssq[warp] = ss;  // read after phase 1's CTA barrier
     }
-    // ok is warp-uniform between CTA barriers (every stage wait is decided for
-    // the whole warp) and CTA-uniform right after each of them (a failure
-    // anywhere in the CTA sets T.fail, read after the barrier)
     bool ok = true;
     int q = 0;
-    volatile int *fail = &T.fail;
-    auto cta_sync = [&]() {
-        named_bar_sync(1, kNCT);
-        ok = ok && *fail == 0;
-    };
 
     auto release = [&](int s) {
         __syncwarp();
@@ -548,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         const int s = q % nstages;
         if (!mbar_wait_warp(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
             ok = false;
-            *fail = 1;
+            T.fail = 1;
             break;
         }
         const uint8_t *st = stages + (size_t)s * stage_bytes;
@@ -571,12 +568,36 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         release(s);
     }
-    cta_sync();
+    named_bar_sync(1, kNCT);
+    // chained input: 1 / rms of v (the per-warp sums of squares were written
+    // before phase 1); h and x are scaled by it, x_out gets this CTA's slice
+    float xs = 1.f;
+    if (p.x_prev) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNCW; ++w) tot += T.ssq[w];
+        const float rms = sqrtf(tot / (float)d);
+        xs = rms > 0.f ? 1.f / rms : 0.f;
+    }
     if (t < nP1r) {
         float z = 0.f;
 #pragma unroll
         for (int w = 0; w < kNCW; ++w) z += T.redp[t][w];
-        p.h[hk0 + t] = fmaxf(z, 0.f);
+        p.h[hk0 + t] = fmaxf(z, 0.f) * xs;
+    }
+    if (p.x_prev) {
+#pragma unroll
+        for (int u = 0; u < CH; ++u)
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) xr[u][e] *= xs;
+        const int nvec = d / 4;
+        const int v0 = (int)((long long)nvec * c / G), v1 = (int)((long long)nvec * (c + 1) / G);
+        if (v0 + t < v1) {
+            const float4 a = reinterpret_cast<const float4 *>(p.x_prev)[v0 + t];
+            const float4 b = reinterpret_cast<const float4 *>(p.y_prev)[v0 + t];
+            reinterpret_cast<float4 *>(p.x_out)[v0 + t] =
+                make_float4((a.x + b.x) * xs, (a.y + b.y) * xs, (a.z + b.z) * xs, (a.w + b.w) * xs);
+        }
     }
     // y = b_down + residual for this CTA's share (loaded right after the
     // wait, stored here; ordered before every CTA's atomics by barrier A)
@@ -593,12 +614,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         p.ctrl->q_done[qpar] = 0u;
     }
     if (t == 0) {
-        if (!grid_barrier(&p.ctrl->bar_ctr, base + (unsigned long long)G, ok, plim, err)) *fail = 1;
+        if (!grid_barrier(&p.ctrl->bar_ctr, base + (unsigned long long)G, ok, p.ctrl, err)) T.fail = 1;
         // every CTA has read this launch's sequence number: move it on (also
         // after a failure, so the sequence stays in step with the counter)
         if (c == 0) atomicAdd(&p.ctrl->bar_seq, 1u);
     }
-    cta_sync();
+    named_bar_sync(1, kNCT);
+    if (*reinterpret_cast<volatile int *>(&T.fail)) ok = false;  // the same decision in every consumer thread
     for (int k = t; k < r; k += kNCT) T.hs[k] = ld_cg_f32(p.h + k);
     named_bar_sync(1, kNCT);
     // this lane's slices of h for the P2 rows, kept in registers (the first
@@ -612,9 +634,8 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         for (int e = 0; e < PEPC; ++e) hreg[u][e] = (lane + 32 * u < nc2) ? T.hs[(lane + 32 * u) * PEPC + e] : 0.f;
 
     // ---- 2. logits of this CTA's neuron range: each warp takes whole P2 jobs
-    //         (a full stage, up to 16 rows) round-robin and works through a job
-    //         8 rows at a time, keeping those rows in flight and reducing them
-    //         together with one transposed butterfly (9 shuffles) ----
+    //         (up to 8 rows) round-robin, keeps all rows in flight, and reduces
+    //         the rows together with one transposed butterfly (9 shuffles) ----
     {
         static_assert(kGroup == 8, "butterfly below reduces 8 rows");
         // Rounds of m <= #stages jobs, one per warp, with a consumer barrier
@@ -624,63 +645,58 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         const int q0 = q;
         const int mr = min(kNCW, nstages);
         for (int i0 = 0; i0 < nP2; i0 += mr) {  // uniform trip count: every warp meets every barrier
-            if (i0 > 0) cta_sync();
+            if (i0 > 0) named_bar_sync(1, kNCT);
             const int i = i0 + warp;
             if (!ok || warp >= mr || i >= nP2) continue;
             const int qq = q0 + i;
             const int s = qq % nstages;
             if (!mbar_wait_warp(&T.full[s], (unsigned)(qq / nstages) & 1u, err)) {
                 ok = false;
-                *fail = 1;
+                T.fail = 1;
                 continue;
             }
             const uint8_t *st = stages + (size_t)s * stage_bytes;
             const int4 job = T.job[s];
             const int nrow = job.z - job.y;
-            for (int h0 = 0; h0 < nrow; h0 += kGroup) {  // warp-uniform
-                const uint8_t *sh = st + (size_t)h0 * p2row;
-                const int nh = min(kGroup, nrow - h0);
-                // All 8 rows, branch-free apart from rows past the job's end
-                // (not read, so no read leaves the stage), so their loads and FMA
-                // chains interleave; chunks past the row end load zeros.
-                float v[kGroup];
+            // All 8 rows, branch-free, so their loads and FMA chains
+            // interleave: rows past nrow read stage bytes that are in bounds
+            // and are discarded; chunks past the row end load zeros.
+            float v[kGroup];
 #pragma unroll
-                for (int rr = 0; rr < kGroup; ++rr) v[rr] = 0.f;
+            for (int rr = 0; rr < kGroup; ++rr) v[rr] = 0.f;
 #pragma unroll
-                for (int u = 0; u < kHreg; ++u) {
-                    const bool in = lane + 32 * u < nc2;
+            for (int u = 0; u < kHreg; ++u) {
+                const bool in = lane + 32 * u < nc2;
 #pragma unroll
-                    for (int rr = 0; rr < kGroup; ++rr) {
-                        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                        if (in && rr < nh) w = *reinterpret_cast<const uint4 *>(sh + (size_t)rr * p2row + (size_t)(lane + 32 * u) * 16);
-                        v[rr] += dot16<PT>(w, hreg[u]);
-                    }
+                for (int rr = 0; rr < kGroup; ++rr) {
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (in) w = *reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)(lane + 32 * u) * 16);
+                    v[rr] += dot16<PT>(w, hreg[u]);
                 }
-                for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {  // ranks above 32*kHreg*PEPC
-#pragma unroll
-                    for (int rr = 0; rr < kGroup; ++rr)
-                        if (rr < nh)
-                            v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(sh + (size_t)rr * p2row + (size_t)cc * 16),
-                                               &T.hs[cc * PEPC]);
-                }
-                // lanes exchange halves of their row set: after the three steps
-                // lane l holds row 4*b4 + 2*b3 + b2 (bits of l) summed over the 8
-                // lanes sharing those bits; two more steps finish the sum
-#pragma unroll
-                for (int m = 16, n = kGroup / 2; m >= 4; m >>= 1, n >>= 1) {
-                    const bool upper = (lane & m) != 0;
-#pragma unroll
-                    for (int k = 0; k < n; ++k) {
-                        const float send = upper ? v[k] : v[k + n];
-                        const float keep = upper ? v[k + n] : v[k];
-                        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-                    }
-                }
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-                const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-                if ((lane & 3) == 0 && rr < nh) T.lg[job.y + h0 + rr - j0] = v[0] + T.pb[job.y + h0 + rr - j0];
             }
+            for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {  // ranks above 32*kHreg*PEPC
+#pragma unroll
+                for (int rr = 0; rr < kGroup; ++rr)
+                    v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)cc * 16),
+                                       &T.hs[cc * PEPC]);
+            }
+            // lanes exchange halves of their row set: after the three steps
+            // lane l holds row 4*b4 + 2*b3 + b2 (bits of l) summed over the 8
+            // lanes sharing those bits; two more steps finish the sum
+#pragma unroll
+            for (int m = 16, n = kGroup / 2; m >= 4; m >>= 1, n >>= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int k = 0; k < n; ++k) {
+                    const float send = upper ? v[k] : v[k + n];
+                    const float keep = upper ? v[k + n] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+            if ((lane & 3) == 0 && rr < nrow) T.lg[job.y + rr - j0] = v[0] + T.pb[job.y + rr - j0];
             // the stage's empty barrier counts one arrival per consumer warp:
             // this warp consumed it alone, so it arrives for all of them
             __syncwarp();
@@ -688,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         q = q0 + nP2;
     }
-    cta_sync();
+    named_bar_sync(1, kNCT);
+    if (*reinterpret_cast<volatile int *>(&T.fail)) ok = false;
     // after a failure no neuron is published (the logits are not valid)
     const int nw = (nR + 31) >> 5;
     for (int wd = warp; wd < nw; wd += kNCW) {
@@ -719,12 +736,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
             const unsigned bits = T.words[wd];
             if ((bits >> lane) & 1u) {
                 const int k = (int)T.wpre[wd] + __popc(bits & ((1u << lane) - 1u));
-                if (k < own) T.j[k] = j0 + wd * 32 + lane;
+                if (k < own) T.j[npf + k] = j0 + wd * 32 + lane;
             }
         }
+        for (int i = t; i < npf; i += kNCT) T.j[i] = pf0 + i;  // the prefix slice first
         named_bar_sync(1, kNCT);
         if (t == 0) {
-            T.share_n = ok ? own : 0;
+            T.share_n = ok ? npf + own : 0;
             mbar_arrive(&T.share_ready);
             // queue slots for the range's k-th active neuron, k >= own: qbase + k
             T.qbase = T.count > own ? atomicAdd(&p.ctrl->q_tail[qpar], (unsigned)(T.count - own)) - (unsigned)own : 0u;
@@ -761,9 +779,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     named_bar_sync(1, kNCT);
     if (t == 0) {
         p.status[c] = (unsigned)T.count;
-        if (!grid_barrier(&p.ctrl->bar_ctr, base + 2ull * (unsigned long long)G, ok, plim, err)) *fail = 1;
+        if (!grid_barrier(&p.ctrl->bar_ctr, base + 2ull * (unsigned long long)G, ok, p.ctrl, err)) T.fail = 1;
     }
-    cta_sync();
+    named_bar_sync(1, kNCT);
+    if (*reinterpret_cast<volatile int *>(&T.fail)) ok = false;
     // every range's count -> exclusive prefix and total
     for (int i = t; i < G; i += kNCT) T.pref[i] = (int)ld_cg_int(reinterpret_cast<const int *>(p.status) + i);
     named_bar_sync(1, kNCT);
@@ -794,32 +813,37 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         }
         if (t == 0) {
             T.total = total;
-            if (c == G - 1 && p.n_active && ok) *p.n_active = total;
+            if (c == G - 1 && p.n_active && ok) *p.n_active = H + total;
         }
     }
     named_bar_sync(1, kNCT);
     // after a failure the counts are not this launch's: no list, no share
     const int n = ok ? T.total : 0;
-    if (p.idx_out && ok) {  // this range's part of the ordered active list
-        for (int i = t; i < T.count; i += kNCT) p.idx_out[T.pref[c] + i] = p.cand[j0 + i];
+    if (p.idx_out && ok) {  // the prefix slice and this range's part of the ordered active list
+        for (int i = t; i < npf; i += kNCT) p.idx_out[pf0 + i] = pf0 + i;
+        for (int i = t; i < T.count; i += kNCT) p.idx_out[H + T.pref[c] + i] = p.cand[j0 + i];
     }
-    // this CTA's balanced share of the active list
+    // this CTA's share: its prefix slice, then its balanced share of the tail's list
     const int k0 = (int)((long long)n * c / G), k1 = (int)((long long)n * (c + 1) / G);
-    const int sn = min(k1 - k0, kMaxShare);
-    for (int i = t; i < sn; i += kNCT) {
+    const int sn = ok ? npf + min(k1 - k0, kMaxShare - npf) : 0;
+    for (int i = t; i < npf && ok; i += kNCT) {
+        T.j[i] = pf0 + i;
+        T.bias[i] = p.b_act ? p.b_act[pf0 + i] : 0.f;
+    }
+    for (int i = t; i < sn - npf; i += kNCT) {
         const int k = k0 + i;
         int lo = 0, hi = G - 1;  // last range whose prefix <= k
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (T.pref[mid] <= k) lo = mid; else hi = mid - 1;
         }
-        const int at = (int)((long long)F * lo / G) + (k - T.pref[lo]);
-        T.j[i] = ld_cg_int(p.cand + at);
-        T.bias[i] = ld_cg_f32(p.cand_bias + at);
+        const int at = H + (int)((long long)(F - H) * lo / G) + (k - T.pref[lo]);
+        T.j[npf + i] = ld_cg_int(p.cand + at);
+        T.bias[npf + i] = ld_cg_f32(p.cand_bias + at);
     }
     named_bar_sync(1, kNCT);
     if (t == 0) {
-        T.share_n = ok ? sn : 0;
+        T.share_n = sn;
         mbar_arrive(&T.share_ready);
     }
     }  // ordered-list mode
@@ -828,10 +852,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     bool any = false;
     while (ok) {
         const int s = q % nstages;
-        if (!mbar_wait_warp(&T.full[s], (unsigned)(q / nstages) & 1u, err)) {
-            *fail = 1;
-            break;
-        }
+        if (!mbar_wait(&T.full[s], (unsigned)(q / nstages) & 1u, err)) break;
         const int4 job = T.job[s];
         if (job.x == kJobEnd) {
             release(s);
@@ -938,9 +959,11 @@ int chunks_per_thread(int wtype, int d)
 
 }  // namespace
 
-bool fused_layer_supported(int wtype, int ptype, int d, int F, int r)
+bool fused_layer_supported(int wtype, int ptype, int d, int F, int r, int prefix)
 {
     const int G = sm_count();
+    // a CTA's share table holds its prefix slice and its share of the tail's list
+    if ((prefix + G - 1) / G + (F - prefix + G - 1) / G > kMaxShare) return false;
     if (G > kMaxG || r > kMaxRank || (r + G - 1) / G > kMaxP1R) return false;
     if ((d / 4 + G - 1) / G > kNCT) return false;  // y initialisation: one float4 per consumer thread
     if (!((wtype == 1 && ptype == 1) || (wtype == 2 && ptype == 1) || (wtype == 0 && ptype == 0))) return false;
@@ -979,50 +1002,19 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     p.r = a.r;
     p.act = a.act;
     p.tau = a.tau;
-    // queue mode needs every active neuron to fit the CTAs' share tables: a CTA
-    // takes no more queue rows once fewer than kQTake slots are left, so all
-    // CTAs together always hold at least (kMaxShare - kQTake + 1) rows each
     p.queue = (!a.idx_out && !a.n_active && (long long)a.F <= (long long)(kMaxShare - kQTake + 1) * G) ? 1 : 0;
+    p.prefix = a.prefix;
     for (int k = 0; k < 2; ++k) {
         p.pf[k] = static_cast<const uint8_t *>(a.pf[k]);
         p.pf_bytes[k] = a.pf[k] ? a.pf_bytes[k] : 0;
     }
     const int esz = a.ptype == 1 ? 2 : 4;
     const uint32_t R = row_slot_bytes(a.wtype, a.d);
+    uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
+    sb = (sb + 127u) & ~127u;
     const int need = chunks_per_thread(a.wtype, a.d);
     const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
-    const size_t budget = (size_t)(colocate(epc, need) ? 110 : 216) * 1024;
-    // Stage size: a P1 row, the FFN rows of one neuron, and a P2 job of at
-    // least 8 rows.  Larger P2 jobs (up to 16 rows, a full stage) are taken
-    // when they cut the logits phase's rounds (one job per consumer warp per
-    // round) without leaving the ring fewer than 9 stages (or its size with
-    // 8-row jobs, when that is already smaller).
-    const uint32_t p2b = (uint32_t)a.r * esz;
-    const uint32_t base = std::max<uint32_t>((uint32_t)a.d * esz, (a.gated ? 2u : 1u) * R);
-    auto stages_of = [&](uint32_t b) {
-        b = (b + 127u) & ~127u;
-        return (int)std::min<size_t>(kMaxStages, (budget - kHdr) / b);
-    };
-    uint32_t sb = std::max<uint32_t>(base, (uint32_t)kGroup * p2b);
-    {
-        const int floor_ns = std::min(stages_of(sb), 9);
-        const int nr = (a.F + G - 1) / G;
-        int best = 1 << 30;
-        uint32_t pick = sb;
-        for (int rjc = kGroup; rjc <= kMaxRJ; ++rjc) {
-            const uint32_t b = std::max<uint32_t>(base, (uint32_t)rjc * p2b);
-            const int nsc = stages_of(b);
-            if (nsc < floor_ns || nsc < 2) continue;
-            const int jobs = (nr + rjc - 1) / rjc, mr = std::min(kNCW, nsc);
-            const int rounds = (jobs + mr - 1) / mr;
-            if (rounds < best) {
-                best = rounds;
-                pick = b;
-            }
-        }
-        sb = pick;
-    }
-    sb = (sb + 127u) & ~127u;
+    const size_t budget = (size_t)(colocate(epc, need) ? 110 : 226) * 1024;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;

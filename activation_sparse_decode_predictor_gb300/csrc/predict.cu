@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_pred_logits(PredParams p)
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
                     if (b < p.B) on = on || (lg[b * kChunk + row] > p.tau);
+                on = on || r0 + ch0 + row < p.prefix;  // always-on prefix
                 if (p.mask) p.mask[r0 + ch0 + row] = on ? 1 : 0;
             }
             const unsigned bits = __ballot_sync(0xffffffffu, on);

@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
                         on = on || l > p.tau;
                     }
                 const int other = __shfl_xor_sync(0xffffffffu, on ? 1 : 0, 1);  // the row's other 4 tokens
-                on = on || other != 0;
+                on = on || other != 0 || k < p.prefix;  // always-on prefix
                 if (valid && rtb == 0) p.out_mask[k] = on ? 1 : 0;
             }
         };
@@ -970,6 +970,7 @@ cudaError_t launch_pred_union(const UnionPredArgs &a, cudaStream_t s)
     q.out_h = nullptr;
     q.p_bias = a.p_bias;
     q.tau = a.tau;
+    q.prefix = a.prefix;
     q.out_logits = a.logits;
     q.out_mask = a.mask;
     return a.B > 4 ? launch_up<PI_F16, false, 2, kEpiLogits>(q, s) : launch_up<PI_F16, false, 1, kEpiLogits>(q, s);

@@ -66,6 +66,9 @@ def parse():
                     help="multi-layer workloads: time one layer on rotating copies instead of the stack")
     ap.add_argument("--batch", type=int, default=0,
                     help="tokens decoded together through the union path (default: the workload's)")
+    ap.add_argument("--dense-prefix", default="0",
+                    help="always-on prefix of the hot-first order: a neuron count, or 'auto' for the neurons that "
+                         "fired on more than half of the profiling tokens (implies the hot-first order)")
     return ap.parse_args()
 
 
@@ -176,15 +179,17 @@ def dist_env():
 
 
 # ------------------------------------------------------------------------------------ workload
-def needed_bytes(w, n_pred, n_down, batch=1):
+def needed_bytes(w, n_pred, n_down, batch=1, prefix=0):
     """Algorithmic bytes of one group of `batch` tokens through one layer:
-    predictor weights (read once for the group), the predicted (union) rows of
-    the up/gate projections (+4 B of index each), the down rows of neurons whose
-    activation is non-zero for at least one token, x in and y out."""
+    predictor weights (read once for the group; no P2 rows for an always-on
+    prefix), the predicted (union) rows of the up/gate projections (+4 B of
+    index each; the prefix rows are part of that list), the down rows of
+    neurons whose activation is non-zero for at least one token, x in and y
+    out."""
     s_p = 4 if w.wtype == "f32" else 2
     R = {"f32": 4 * w.d_model, "f16": 2 * w.d_model, "q4_0": w.d_model // 32 * 18}[w.wtype]
     g = 2 if w.gated else 1
-    pred = (w.rank * w.d_model + w.d_ff * w.rank) * s_p
+    pred = (w.rank * w.d_model + (w.d_ff - prefix) * w.rank) * s_p
     ffn = n_pred * (R * g + 4) + n_down * R + batch * w.d_model * 4 * 2
     return pred, ffn
 
@@ -205,15 +210,19 @@ def top_share(counts, frac=0.26):
     return float(c[:k].sum() / max(1.0, c.sum()))
 
 
-def hot_first(w, L0, dev):
+def hot_first(w, L0, dev, prefix="0"):
     """Offline profiling pass: w.profile_tokens synthetic tokens (a token stream
-    of their own) through pi_fire_counts on the layer as generated, the
-    hot-first order from pi_hot_first_perm, then every per-neuron array (rows of
-    w_up / w_gate / w_down / p2, entries of b_act / p_bias) permuted with
-    pi_permute_rows.  Returns the permuted layer and statistics of the order."""
+    of their own; 1024 when the workload names none) through pi_fire_counts on
+    the layer as generated, the hot-first order from pi_hot_first_perm, then
+    every per-neuron array (rows of w_up / w_gate / w_down / p2, entries of
+    b_act / p_bias) permuted with pi_permute_rows.  An always-on prefix is set
+    from `prefix` (a count, or 'auto': the neurons that fired on more than half
+    of the profiling tokens).  Returns the permuted layer and statistics of
+    the order."""
     F = w.d_ff
     lay = B.Layer.from_dict(L0)
-    Xp = synth.workload_tokens(w, n=w.profile_tokens, device=f"cuda:{dev}", stream=1)
+    T = w.profile_tokens or 1024
+    Xp = synth.workload_tokens(w, n=T, device=f"cuda:{dev}", stream=1)
     counts = torch.zeros(F, dtype=torch.int32, device=Xp.device)
     B.pi_fire_counts(lay, Xp, counts)
     c = counts.cpu().numpy()
@@ -225,17 +234,20 @@ def hot_first(w, L0, dev):
             out[k] = B.pi_permute_rows(L0[k], perm_d)
     torch.cuda.synchronize()
     cs = c[perm].astype(np.float64)
-    stats = {"profile_tokens": int(w.profile_tokens),
-             "first_quarter_share_profile": float(cs[: F // 4].sum() / max(1.0, cs.sum()))}
+    H = int(np.sum(c > T // 2)) if prefix == "auto" else int(prefix)
+    out["dense_prefix"] = H
+    stats = {"profile_tokens": int(T),
+             "first_quarter_share_profile": float(cs[: F // 4].sum() / max(1.0, cs.sum())),
+             "dense_prefix": H}
     return out, perm, stats
 
 
-def setup_ours(w, replicas, dev):
+def setup_ours(w, replicas, dev, prefix="0"):
     torch.cuda.set_device(dev)
     L0 = synth.workload_layer(w, 0, device=f"cuda:{dev}")
     perm_stats = None
-    if w.permute:
-        L0, _, perm_stats = hot_first(w, L0, dev)
+    if w.permute or prefix != "0":
+        L0, _, perm_stats = hot_first(w, L0, dev, prefix)
     if w.wtype == "q4_0":
         # the generator returns fp16 matrices; store them as Q4_0 with the library's quantiser
         for k in ("w_up", "w_gate", "w_down"):
@@ -497,7 +509,8 @@ def run_ours(args, w):
     dev = local
     torch.cuda.set_device(dev)
     B.lib()
-    L0, reps, X, perm_stats = setup_ours(w, args.replicas, dev)
+    L0, reps, X, perm_stats = setup_ours(w, args.replicas, dev, args.dense_prefix)
+    H = int(L0.get("dense_prefix", 0))
     if args.tokens:
         X = X[:args.tokens].contiguous()
     bsz = args.batch or w.batch
@@ -514,7 +527,7 @@ def run_ours(args, w):
 
     # statistics of the active sets (outside any timed region)
     S = active_stats(w, L0, reps[0][1], X, ws, ws1, bsz)
-    pred_b, ffn_b = needed_bytes(w, S["n_pred"], S["n_down"], bsz)
+    pred_b, ffn_b = needed_bytes(w, S["n_pred"], S["n_down"], bsz, H)
     bytes_grp = pred_b + ffn_b                       # per group, arrays
     mean_bytes = float(np.mean(bytes_grp)) / bsz     # per token
     fire = S["true"].sum(dim=0).cpu().numpy()
@@ -634,7 +647,8 @@ def run_ours(args, w):
 
     if rank == 0:
         cfg = workload_config(w, bsz, False)
-        cfg.update({"tokens_per_step": T, "layer_replicas": len(reps),
+        cfg["hot_first_order"] = bool(perm_stats)
+        cfg.update({"dense_prefix": H, "tokens_per_step": T, "layer_replicas": len(reps),
                     "l2": f"inputs larger than L2: {len(reps)} rotating layer copies, "
                           f"{len(reps) * mean_bytes / 1e6:.0f} MB needed bytes per rotation",
                     "n_active_mean": float(np.mean(S["n_pred"])), "n_nonzero_mean": float(np.mean(S["n_down"])),
@@ -687,6 +701,11 @@ def run_stack(args, w):
     B.lib()
     nl = w.layers
     Ls = [synth.workload_layer(w, l, device=f"cuda:{dev}") for l in range(nl)]
+    stack_prefix = []
+    if args.dense_prefix != "0":  # hot-first order and an always-on prefix for every layer
+        for l in range(nl):
+            Ls[l], _, st_ = hot_first(w, Ls[l], dev, args.dense_prefix)
+            stack_prefix.append(st_["dense_prefix"])
     lays = [B.Layer.from_dict(L) for L in Ls]
     for l in range(nl):
         lays[l].set_next(lays[(l + 1) % nl])  # the next layer of the stack (layer 0 of the next token)
@@ -738,7 +757,8 @@ def run_stack(args, w):
         fire.append(S["true"].sum(dim=0).cpu().numpy())
         trues.append(S["true"])
     n_pred, n_down = np.concatenate(n_pred), np.concatenate(n_down)
-    pred_b, ffn_b = needed_bytes(w, n_pred, n_down, 1)
+    Hm = float(np.mean(stack_prefix)) if stack_prefix else 0.0
+    pred_b, ffn_b = needed_bytes(w, n_pred, n_down, 1, Hm)
     mean_bytes = float(np.mean(pred_b + ffn_b))  # per token and layer
 
     g_step = capture(step, stream)
@@ -821,6 +841,9 @@ def run_stack(args, w):
     if rank == 0:
         fire_all = np.concatenate(fire)
         cfg = workload_config(w, 1, True)
+        if stack_prefix:
+            cfg["hot_first_order"] = True
+            cfg["dense_prefix_per_layer"] = stack_prefix
         cfg.update({"tokens_per_step": T,
                     "l2": f"inputs larger than L2: {nl} distinct layers, "
                           f"{nl * mean_bytes / 1e6:.0f} MB needed bytes per token",

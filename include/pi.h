@@ -87,7 +87,7 @@ typedef void *pi_stream; /* cudaStream_t */
  *   predictor (d -> rank, ReLU, rank -> d_ff; the pages give its purpose, not
  *   its form, and this low-rank form is the reading taken):
  *     h_k = max(p1[k].x, 0),  logit_j = p2[j].h + p_bias[j],  neuron j is
- *     predicted active when logit_j > threshold.
+ *     predicted active when j < dense_prefix or logit_j > threshold.
  *
  * Storage:
  *   wtype PI_F32 / PI_F16: w_up, w_gate, w_down are [d_ff][d_model].
@@ -128,6 +128,15 @@ typedef struct pi_ffn_desc_s {
      * aligned is skipped).  Layer-by-layer decode knows its next layer; the
      * weights are still read from HBM once. */
     const struct pi_ffn_desc_s *next;
+    /* Always-on prefix: neurons [0, dense_prefix) of the storage order are
+     * active at every step whatever the predictor says, and their rows of p2
+     * and p_bias are not read by the one-kernel layer step.  With the
+     * hot-first order (pi_hot_first_perm) these are the neurons an offline
+     * profile found to fire most often -- the pages' hot neurons, which the
+     * method keeps on the fast device (PowerInfer summary page, "方法详解"
+     * method detail) -- so the predictor only decides the cold tail.
+     * 0 <= dense_prefix <= d_ff; 0 = none. */
+    int32_t dense_prefix;
 } pi_ffn_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -43,7 +43,7 @@ class _Layer(ctypes.Structure):
         ("w_up", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
         ("b_act", ctypes.c_void_p), ("b_down", ctypes.c_void_p),
         ("p1", ctypes.c_void_p), ("p2", ctypes.c_void_p), ("p_bias", ctypes.c_void_p),
-        ("threshold", ctypes.c_double),
+        ("threshold", ctypes.c_double), ("dense_prefix", ctypes.c_int64),
     ]
 
 
@@ -119,7 +119,7 @@ class Layer:
     """
 
     def __init__(self, d_model, d_ff, rank, w_up, w_down, w_gate=None, b_act=None, b_down=None,
-                 p1=None, p2=None, p_bias=None, threshold=0.0, act=ACT_RELU):
+                 p1=None, p2=None, p_bias=None, threshold=0.0, act=ACT_RELU, dense_prefix=0):
         self.d_model, self.d_ff, self.rank = int(d_model), int(d_ff), int(rank)
         self.gated = w_gate is not None
         self.wtype = _wtype_of(np.asarray(w_up))
@@ -134,12 +134,13 @@ class Layer:
         self.p_bias = _c(p_bias, np.float32)
         self.threshold = float(threshold)
         self.act = int(act)
+        self.dense_prefix = int(dense_prefix)
         self._check()
         self._s = _Layer(self.d_model, self.d_ff, self.rank, int(self.gated), self.act,
                          self.wtype, self.ptype,
                          _ptr(self.w_up), _ptr(self.w_gate), _ptr(self.w_down),
                          _ptr(self.b_act), _ptr(self.b_down),
-                         _ptr(self.p1), _ptr(self.p2), _ptr(self.p_bias), self.threshold)
+                         _ptr(self.p1), _ptr(self.p2), _ptr(self.p_bias), self.threshold, self.dense_prefix)
 
     def _check(self):
         d, F = self.d_model, self.d_ff
@@ -154,6 +155,7 @@ class Layer:
         if self.p1 is not None:
             assert self.p1.shape == (self.rank, d) and self.p2.shape == (F, self.rank)
             assert self.ptype in (F32, F16)
+        assert 0 <= self.dense_prefix <= F
 
 
 def q4_0_bytes(rows: int, cols: int) -> int:
@@ -218,7 +220,8 @@ def true_mask(L: Layer, x: np.ndarray):
 
 
 def predict(L: Layer, x: np.ndarray):
-    """(h, logit, mask) of the low-rank predictor for one token."""
+    """(h, logit, mask) of the low-rank predictor for one token; neurons below
+    the layer's dense_prefix are always in the mask."""
     x = _c(x, np.float32)
     h = np.empty(L.rank, dtype=np.float64)
     logit = np.empty(L.d_ff, dtype=np.float64)
@@ -289,6 +292,7 @@ def neuron_shard(L: Layer, neurons: np.ndarray, keep_b_down: bool) -> Layer:
             return np.concatenate([codes.ravel(), scales.ravel()])
         return np.ascontiguousarray(a[neurons])
 
+    assert L.dense_prefix == 0, "a neuron shard of a layer with an always-on prefix is not defined"
     return Layer(d, neurons.size, L.rank, rows(L.w_up), rows(L.w_down), w_gate=rows(L.w_gate),
                  b_act=rows(L.b_act), b_down=L.b_down if keep_b_down else None, p1=L.p1, p2=rows(L.p2),
                  p_bias=rows(L.p_bias), threshold=L.threshold, act=L.act)

@@ -53,6 +53,7 @@ typedef struct {
     const void *p1, *p2;
     const float *p_bias;  /* [d_ff] or NULL */
     double threshold;
+    int64_t dense_prefix; /* neurons [0, dense_prefix) are always active */
 } oracle_layer;
 
 /* ------------------------------------------------------------------------- */
@@ -273,7 +274,12 @@ void oracle_true_mask(const oracle_layer *L, const float *x, uint8_t *mask, doub
  * without giving its form; the reading taken is d -> r, ReLU, r -> d_ff):
  *   h_k     = max(sum_i P1[k,i] x_i, 0)
  *   logit_j = sum_k P2[j,k] h_k + p_bias_j
- *   mask_j  = logit_j > threshold                                            */
+ *   mask_j  = logit_j > threshold
+ * With an always-on prefix (the pages' split of a layer into hot neurons,
+ * found offline and kept on the fast device, and cold ones -- summary page,
+ * "方法详解" method detail; here the first dense_prefix neurons of the
+ * hot-first order are computed every step): mask_j = 1 for j < dense_prefix,
+ * whatever the logit.                                                        */
 void oracle_predict(const oracle_layer *L, const float *x, double *h, double *logit, uint8_t *mask)
 {
     ensure_table();
@@ -289,7 +295,7 @@ void oracle_predict(const oracle_layer *L, const float *x, double *h, double *lo
             s += elem(L->p2, L->ptype, L->d_ff, L->rank, j, k) * h[k];
         if (L->p_bias) s += (double)L->p_bias[j];
         logit[j] = s;
-        if (mask) mask[j] = s > L->threshold ? 1 : 0;
+        if (mask) mask[j] = (j < L->dense_prefix || s > L->threshold) ? 1 : 0;
     }
 }
 

@@ -48,7 +48,7 @@ def test_status_strings(L):
 def _desc(**kw):
     d = dict(d_model=512, d_ff=2048, rank=64, gated=0, act=0, wtype=B.PI_F16, ptype=B.PI_F16, threshold=0.0,
              w_up=0x1000, w_gate=None, w_down=0x2000, b_act=None, b_down=None, p1=0x3000, p2=0x4000, p_bias=None,
-             next=None)
+             next=None, dense_prefix=0)
     d.update(kw)
     return B.FFNDesc(*[d[f] for f, _ in B.FFNDesc._fields_])
 
@@ -78,6 +78,8 @@ def test_validation_before_launch(L):
     assert _call_layer(L, _desc(), ws=0x40010) == 4                    # workspace alignment
     assert _call_layer(L, _desc(), ws_bytes=16) == 8
     assert _call_layer(L, _desc(wtype=B.PI_F32), batch=2) == 3         # union path is fp16 / Q4_0
+    assert _call_layer(L, _desc(dense_prefix=-1)) == 2                 # always-on prefix out of range
+    assert _call_layer(L, _desc(dense_prefix=2049)) == 2
 
 
 def test_compact_validation(L):

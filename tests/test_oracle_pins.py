@@ -247,6 +247,26 @@ def test_projection_predictor_identity():
                                    atol=1e-11)
 
 
+@pytest.mark.parametrize("prefix", [0, 1, 37, 120])
+def test_always_on_prefix_in_the_predicted_mask(prefix):
+    """Neurons below dense_prefix are in the mask whatever their logit; the
+    others follow the float64 formula.  The whole layer as prefix gives the
+    all-ones mask, and so the dense FFN, bitwise."""
+    lay, w = _np_layer(64, 120, 24, False, "f16", seed=43)
+    lay_p = oracle.Layer(64, 120, 24, w["w_up"], w["w_down"], b_act=w["b_act"], b_down=w["b_down"] + 0.25,
+                         p1=w["p1"], p2=w["p2"], p_bias=w["p_bias"], threshold=0.0, dense_prefix=prefix)
+    p1 = w["p1"].astype(np.float64)
+    p2 = w["p2"].astype(np.float64)
+    for x in synth.tokens(3, 64, 44).numpy():
+        _, logit, mask = oracle.predict(lay_p, x)
+        ref = (p2 @ np.maximum(p1 @ x.astype(np.float64), 0.0)) > 0.0
+        ref[:prefix] = True
+        assert np.array_equal(mask.astype(bool), ref)
+        if prefix == 120:
+            y = oracle.sparse_ffn(lay_p, x, oracle.compact(mask))
+            assert np.array_equal(y, oracle.dense_ffn(lay, x))
+
+
 def test_predict_union_is_or_of_tokens():
     lay, _ = _np_layer(32, 100, 8, False, "f32", seed=51)
     X = synth.tokens(5, 32, 52).numpy()
