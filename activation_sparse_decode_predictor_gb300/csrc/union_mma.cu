@@ -28,7 +28,8 @@
 // Kernels (one stream, chained with programmatic dependent launch):
 //   k_union_prep  x -> fp16 hi/lo fragments in mma B-operand order, exponents.
 //   k_union_up    persistent, one CTA per SM.  Work unit = 16 union rows x one
-//                 chunk of d_model (2048 fp16 / 4096 Q4_0 weights) of one
+//                 chunk of d_model (2048 fp16 weights; 4096 Q4_0 weights at
+//                 2-4 tokens, 2048 at 5-8 tokens: up_ks) of one
 //                 matrix; units are ordered chunk-major and dealt out to CTAs in
 //                 contiguous ranges.  The 8 consumer warps split each unit's
 //                 chunk and leave their partial sums in one of 4 shared-memory
@@ -71,6 +72,10 @@ constexpr int kEpiFfn = 0, kEpiHidden = 1, kEpiLogits = 2;  // up kernel epilogu
 // Up-projection chunks (weights of d_model per unit) and shared-memory row strides.
 constexpr int kKsF16 = 2048;
 constexpr int kKsQ4 = 4096;
+// Unit width of the up kernel: Q4_0 at 5-8 tokens (two operand groups) takes
+// 2048-weight units so that each warp's x fragments of a unit (8 steps x 2
+// groups x 16 bytes per lane) stay in registers across the units of a chunk.
+__host__ __device__ constexpr int up_ks(bool q4, int ng) { return q4 ? (ng == 2 ? 2048 : kKsQ4) : kKsF16; }
 // Down-projection column blocks.
 constexpr int kCw = 2048;                  // columns per block (4 KB fp16 row pieces)
 constexpr int kWc = kCw / kUW;             // 256 columns per consumer warp
@@ -320,7 +325,7 @@ template <int WT, bool GATED, int NG, int EPI>
 __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int nstages, int rs, int ss, uint32_t SB)
 {
     constexpr bool Q4 = WT == PI_Q4_0;
-    constexpr int KS = Q4 ? kKsQ4 : kKsF16;   // weights of d_model per unit
+    constexpr int KS = up_ks(Q4, NG);         // weights of d_model per unit
     constexpr int SPW = KS / 32 / kUW;        // 32-wide steps per warp and unit
     constexpr int M = GATED ? 2 : 1;          // matrices per row tile
     // rs, ss: row strides of a stage (code / fp16 rows; Q4_0 scale rows), SB: stage bytes
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
 
     // ---------------------------------- consumer warps ----------------------------------
     const int g = lane >> 2, t = lane & 3;
-    constexpr bool XREG = !(Q4 && NG == 2);  // x fragments held in registers (not for Q4_0 at 5-8 tokens)
+    constexpr bool XREG = SPW * NG <= 16;  // x fragments held in registers (every unit width chosen above)
     uint4 xr[XREG ? SPW : 1][NG];
     int xc = -1;
     for (int jj = 0; jj < cnt; ++jj) {
@@ -868,7 +873,7 @@ cudaError_t launch_up(const SparseParams &p, cudaStream_t s)
 {
     // stages sized by the widest chunk this contraction has (its K may be far below KS)
     constexpr bool Q4 = WT == PI_Q4_0;
-    constexpr int KS = Q4 ? kKsQ4 : kKsF16;
+    constexpr int KS = up_ks(Q4, NG);
     const int kse = p.d < KS ? p.d : KS;
     int rs, ss;
     if (Q4) {
