@@ -237,14 +237,22 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, unsigned parity, u
     return __all_sync(0xffffffffu, got);
 }
 
-// The same copy with an L2 evict-first policy: for weights that one decode
-// step reads once, so their lines leave L2 before data that is read again
-// (the next layer's predictor rows asked into L2 ahead of time, activations,
-// the control block).
-__device__ __forceinline__ void bulk_g2s_once(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+// L2 evict-first policy for weights that one decode step reads once, so their
+// lines leave L2 before data that is read again (the next layer's predictor
+// rows asked into L2 ahead of time, activations, the control block).  Made
+// once per issuing thread: createpolicy is an instruction of its own, and a
+// producer that made it before every copy paid for it on each one.
+__device__ __forceinline__ unsigned long long evict_first_policy()
 {
     unsigned long long pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// bulk_g2s with an L2 cache policy from evict_first_policy().
+__device__ __forceinline__ void bulk_g2s_once(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              unsigned long long pol)
+{
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
             smem_u32(dst)),

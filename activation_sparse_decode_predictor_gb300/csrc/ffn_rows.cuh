@@ -81,18 +81,19 @@ __device__ __forceinline__ void chunk_axpy(const uint8_t *slot, int c, int d, fl
     }
 }
 
-// Issue the bulk copies of one matrix row of neuron j into a stage slot (each
-// row is read once per decode step: evict-first in L2).
+// Issue the bulk copies of one matrix row of neuron j into a stage slot, with
+// the L2 policy `pol` (evict_first_policy(): each row is read once per step).
 template <int WT>
-__device__ __forceinline__ void copy_row(uint8_t *slot, const uint8_t *base, int j, int d, int F, uint64_t *bar)
+__device__ __forceinline__ void copy_row(uint8_t *slot, const uint8_t *base, int j, int d, int F, uint64_t *bar,
+                                         unsigned long long pol)
 {
     if constexpr (WT == 2) {
         const size_t cb = (size_t)d / 2, sb = (size_t)d / 16;
-        bulk_g2s_once(slot, base + (size_t)j * cb, (uint32_t)cb, bar);
-        bulk_g2s_once(slot + cb, base + (size_t)F * cb + (size_t)j * sb, (uint32_t)sb, bar);
+        bulk_g2s_once(slot, base + (size_t)j * cb, (uint32_t)cb, bar, pol);
+        bulk_g2s_once(slot + cb, base + (size_t)F * cb + (size_t)j * sb, (uint32_t)sb, bar, pol);
     } else {
         const size_t rb = (size_t)d * (WT == 0 ? 4 : 2);
-        bulk_g2s_once(slot, base + (size_t)j * rb, (uint32_t)rb, bar);
+        bulk_g2s_once(slot, base + (size_t)j * rb, (uint32_t)rb, bar, pol);
     }
 }
 

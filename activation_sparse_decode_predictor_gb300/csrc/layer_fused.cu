@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
         // loads on this SM while this CTA is still working.
         pdl_trigger();
         if (lane == 0) {
+            const unsigned long long pol = evict_first_policy();
             int q = 0;
             bool failed = false;
             auto acquire = [&](int qq) -> bool {
@@ -293,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                     const uint32_t bytes = (uint32_t)(k1 - k0) * p1row;
                     T.job[s] = make_int4(kJobP1, k0, k1, 0);
                     mbar_arrive_expect_tx(&T.full[s], bytes);
-                    bulk_g2s_once(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s]);
+                    bulk_g2s_once(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s], pol);
                 } else {
                     const int g0 = j0 + (i - nP1) * kGroup, g1 = min(g0 + kGroup, j1);
                     const uint32_t bytes = (uint32_t)(g1 - g0) * p2row;
                     T.job[s] = make_int4(kJobP2, g0, g1, 0);
                     mbar_arrive_expect_tx(&T.full[s], bytes);
-                    bulk_g2s_once(st, p.p2 + (size_t)g0 * p2row, bytes, &T.full[s]);
+                    bulk_g2s_once(st, p.p2 + (size_t)g0 * p2row, bytes, &T.full[s], pol);
                 }
                 ++q;
             }
@@ -423,11 +424,11 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
                 T.job[s] = make_int4(kind, i, j, 0);
                 if (kind == kJobUp) {
                     mbar_arrive_expect_tx(&T.full[s], GATED ? 2u * R : R);
-                    copy_row<WT>(st, p.w_act, j, d, F, &T.full[s]);
-                    if constexpr (GATED) copy_row<WT>(st + R, p.w_up, j, d, F, &T.full[s]);
+                    copy_row<WT>(st, p.w_act, j, d, F, &T.full[s], pol);
+                    if constexpr (GATED) copy_row<WT>(st + R, p.w_up, j, d, F, &T.full[s], pol);
                 } else if (kind == kJobDown) {
                     mbar_arrive_expect_tx(&T.full[s], R);
-                    copy_row<WT>(st, p.w_down, j, d, F, &T.full[s]);
+                    copy_row<WT>(st, p.w_down, j, d, F, &T.full[s], pol);
                 } else {
                     mbar_arrive(&T.full[s]);
                 }

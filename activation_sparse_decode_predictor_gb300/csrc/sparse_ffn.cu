@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_b1(SparseParams p, int n
     if (warp == kNCW) {
         // ------------------------------ producer warp ------------------------------
         int q = 0;  // jobs issued so far (all segments)
+        const unsigned long long pol = evict_first_policy();
         bool failed = false;
         for (int seg = 0; seg < cnt && !failed; seg += kSeg) {
             const int sn = min(kSeg, cnt - seg);
@@ -131,11 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_b1(SparseParams p, int n
                     uint8_t *st = stages + (size_t)s * stage_bytes;
                     if (kind == kJobUp) {
                         mbar_arrive_expect_tx(&T.full[s], GATED ? 2u * R : R);
-                        copy_row<WT>(st, p.w_act, j, d, F, &T.full[s]);
-                        if constexpr (GATED) copy_row<WT>(st + R, p.w_up, j, d, F, &T.full[s]);
+                        copy_row<WT>(st, p.w_act, j, d, F, &T.full[s], pol);
+                        if constexpr (GATED) copy_row<WT>(st + R, p.w_up, j, d, F, &T.full[s], pol);
                     } else if (kind == kJobDown) {
                         mbar_arrive_expect_tx(&T.full[s], R);
-                        copy_row<WT>(st, p.w_down, j, d, F, &T.full[s]);
+                        copy_row<WT>(st, p.w_down, j, d, F, &T.full[s], pol);
                     } else {
                         mbar_arrive(&T.full[s]);
                     }

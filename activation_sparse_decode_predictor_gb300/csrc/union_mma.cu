@@ -512,6 +512,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
     }
 
     if (warp == kUW) {
+        const unsigned long long pol = evict_first_policy();
         auto job_tile = [&](int jj) { return ((u0 + jj) % per) / M; };
         auto job_bytes = [&](int jj) {
             const int len = min(KS, d - ((u0 + jj) / per) * KS);
@@ -526,11 +527,11 @@ __global__ void __launch_bounds__(kUpThreads, 1) k_union_up(SparseParams p, int 
             uint8_t *st = stages + (size_t)s * SB;
             const size_t jn = (size_t)rows[lane];
             if constexpr (Q4) {
-                bulk_g2s_once(st + lane * rs, W + jn * (d / 2) + k0 / 2, (uint32_t)(len / 2), &full[s]);
+                bulk_g2s_once(st + lane * rs, W + jn * (d / 2) + k0 / 2, (uint32_t)(len / 2), &full[s], pol);
                 bulk_g2s_once(st + 16 * rs + lane * ss, W + (size_t)F * (d / 2) + jn * (d / 16) + k0 / 16,
-                         (uint32_t)(len / 16), &full[s]);
+                              (uint32_t)(len / 16), &full[s], pol);
             } else {
-                bulk_g2s_once(st + lane * rs, W + (jn * d + k0) * 2, (uint32_t)len * 2u, &full[s]);
+                bulk_g2s_once(st + lane * rs, W + (jn * d + k0) * 2, (uint32_t)len * 2u, &full[s], pol);
             }
         };
         produce_rows(p, n, cnt, nstages, 0, 0u, full, empty, tab, job_tile, job_bytes, issue, [](int, int) {});
@@ -679,6 +680,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
     if (cnt <= 0) return;
 
     if (warp == kUW) {
+        const unsigned long long pol = evict_first_policy();
         auto job_tile = [&](int jj) { return (int)((u0 + jj) % T); };
         auto job_bytes = [&](int jj) {
             const int nc = min(CW, d - (int)((u0 + jj) / T) * CW);
@@ -691,11 +693,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_union_down(SparseParams p, int
             uint8_t *st = stages + (size_t)s * SB;
             const size_t jn = (size_t)rows[lane];
             if constexpr (Q4) {
-                bulk_g2s_once(st + lane * kRsQ4Dn, p.w_down + jn * (d / 2) + c0 / 2, (uint32_t)(nc / 2), &full[s]);
+                bulk_g2s_once(st + lane * kRsQ4Dn, p.w_down + jn * (d / 2) + c0 / 2, (uint32_t)(nc / 2), &full[s], pol);
                 bulk_g2s_once(st + 16 * kRsQ4Dn + lane * kSsQ4Dn, p.w_down + (size_t)F * (d / 2) + jn * (d / 16) + c0 / 16,
-                         (uint32_t)(nc / 16), &full[s]);
+                              (uint32_t)(nc / 16), &full[s], pol);
             } else {
-                bulk_g2s_once(st + lane * kRsF16Dn, p.w_down + (jn * d + c0) * 2, (uint32_t)nc * 2u, &full[s]);
+                bulk_g2s_once(st + lane * kRsF16Dn, p.w_down + (jn * d + c0) * 2, (uint32_t)nc * 2u, &full[s], pol);
             }
         };
         // the tile's activations (written by the up kernel), one 512-byte copy
