@@ -65,9 +65,13 @@ namespace pi {
 
 namespace {
 
-constexpr int kNCW = 8;
-constexpr int kNCT = kNCW * 32;
-constexpr int kThreads = kNCT + 32;
+// Consumer warps: 8, or 12 for the widest rows.  With 8 warps and x of
+// d_model >= 12 Ki fp16 columns each consumer thread holds 6-8 chunks of x and
+// the per-row dot products run out of independent work; 12 warps take 4-6
+// chunks each (measured on the OPT-175B shape: 52.3 -> 51.0 us per layer;
+// narrower rows are slower with 12, so they keep 8).
+constexpr int kNCW8 = 8;
+constexpr int kMaxNCW = 12;
 constexpr int kMaxStages = 24;
 constexpr int kMaxShare = 512;     // FFN rows per CTA (share of the active list)
 constexpr int kMaxRange = 512;     // neurons per CTA range (P2 rows)
@@ -86,15 +90,15 @@ struct Tables {
     uint64_t empty[kMaxStages];
     uint64_t share_ready;
     int4 job[kMaxStages];
-    float redp[kMaxP1R][kNCW];
-    float redu[kUpRing][kNCW][2];
+    float redp[kMaxP1R][kMaxNCW];
+    float redu[kUpRing][kMaxNCW][2];
     int upcnt[kUpRing];
     unsigned long long seq;
     int share_n;
     int count, total;
     unsigned qbase;     // queue mode: the queue slot of the range's k-th active neuron is qbase + k
-    int wsum[kNCW];
-    float ssq[kNCW];    // chained input: per-warp sums of squares of x_prev + y_prev
+    int wsum[kMaxNCW];
+    float ssq[kMaxNCW];  // chained input: per-warp sums of squares of x_prev + y_prev
     unsigned words[kMaxRange / 32 + 1];
     unsigned wpre[kMaxRange / 32 + 1];
     float lg[kMaxRange];
@@ -209,10 +213,18 @@ struct FusedParams {
 #endif
 __host__ __device__ constexpr bool colocate(int epc, int ch) { return PI_FUSED_COLOCATE && epc * ch <= 16; }
 
-template <int WT, typename PT, bool GATED, int CH>
-__global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
+// Registers: each SM sub-partition's 16 Ki registers hold the warps placed on
+// it.  8 consumer warps + the producer put 3 warps on one sub-partition (at
+// most 170 registers a thread); 12 + 1 put 4 there, so that variant declares a
+// 512-thread bound, which caps it at 128 registers (it launches 416 threads).
+template <int WT, typename PT, bool GATED, int CH, int NCW>
+__global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
 {
+    static_assert(NCW == kNCW8 || NCW == kMaxNCW, "8 or 12 consumer warps");
+    constexpr int kNCW = NCW;
+    constexpr int kNCT = kNCW * 32;
+    constexpr int kThreads = kNCT + 32;
     constexpr int EPC = Fmt<WT>::EPC;                // weight elements per 16-byte chunk
     constexpr int PSEG = EPC * (int)sizeof(PT) / 16; // P1 chunks covering one weight chunk's columns
     constexpr int PEPC = 16 / (int)sizeof(PT);       // predictor elements per 16-byte chunk
@@ -924,10 +936,10 @@ __global__ void __launch_bounds__(kThreads, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     }
 }
 
-template <int WT, typename PT, bool GATED, int CH>
+template <int WT, typename PT, bool GATED, int CH, int NCW>
 cudaError_t launch_t(const FusedParams &p, int G, int ns, uint32_t stage_bytes, cudaStream_t s)
 {
-    auto k = k_layer_b1<WT, PT, GATED, CH>;
+    auto k = k_layer_b1<WT, PT, GATED, CH, NCW>;
     const size_t smem = kHdr + (size_t)ns * stage_bytes;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -935,27 +947,35 @@ cudaError_t launch_t(const FusedParams &p, int G, int ns, uint32_t stage_bytes, 
     // (this layer's and the next one's) fit on an SM
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(G), dim3(kThreads), smem, s, p, ns, stage_bytes);
+    return launch_pdl(k, dim3(G), dim3(NCW * 32 + 32), smem, s, p, ns, stage_bytes);
+}
+
+int chunks_per_thread(int wtype, int d, int ncw)
+{
+    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
+    return (d / epc + ncw * 32 - 1) / (ncw * 32);
 }
 
 template <int WT, typename PT, bool GATED>
-cudaError_t launch_ch(const FusedParams &p, int need, int G, int ns, uint32_t sb, cudaStream_t s)
+cudaError_t launch_ch(const FusedParams &p, int d, int G, int ns, uint32_t sb, cudaStream_t s)
 {
-    if (need <= 1) return launch_t<WT, PT, GATED, 1>(p, G, ns, sb, s);
-    if (need <= 2) return launch_t<WT, PT, GATED, 2>(p, G, ns, sb, s);
+    const int need = chunks_per_thread(WT, d, kNCW8);
     if constexpr (WT != 2) {
-        if (need <= 3) return launch_t<WT, PT, GATED, 3>(p, G, ns, sb, s);
-        if (need <= 4) return launch_t<WT, PT, GATED, 4>(p, G, ns, sb, s);
-        if (need <= 6) return launch_t<WT, PT, GATED, 6>(p, G, ns, sb, s);
-        if (need <= 8) return launch_t<WT, PT, GATED, 8>(p, G, ns, sb, s);
+        if (need >= 6) {  // the widest rows: 12 consumer warps, 4-6 chunks a thread
+            const int need12 = chunks_per_thread(WT, d, kMaxNCW);
+            if (need12 <= 4) return launch_t<WT, PT, GATED, 4, kMaxNCW>(p, G, ns, sb, s);
+            if (need12 <= 6) return launch_t<WT, PT, GATED, 6, kMaxNCW>(p, G, ns, sb, s);
+        }
+    }
+    if (need <= 1) return launch_t<WT, PT, GATED, 1, kNCW8>(p, G, ns, sb, s);
+    if (need <= 2) return launch_t<WT, PT, GATED, 2, kNCW8>(p, G, ns, sb, s);
+    if constexpr (WT != 2) {
+        if (need <= 3) return launch_t<WT, PT, GATED, 3, kNCW8>(p, G, ns, sb, s);
+        if (need <= 4) return launch_t<WT, PT, GATED, 4, kNCW8>(p, G, ns, sb, s);
+        if (need <= 6) return launch_t<WT, PT, GATED, 6, kNCW8>(p, G, ns, sb, s);
+        if (need <= 8) return launch_t<WT, PT, GATED, 8, kNCW8>(p, G, ns, sb, s);
     }
     return cudaErrorNotSupported;
-}
-
-int chunks_per_thread(int wtype, int d)
-{
-    const int epc = wtype == 0 ? 4 : (wtype == 1 ? 8 : 32);
-    return (d / epc + kNCT - 1) / kNCT;
 }
 
 }  // namespace
@@ -966,10 +986,10 @@ bool fused_layer_supported(int wtype, int ptype, int d, int F, int r, int prefix
     // a CTA's share table holds its prefix slice and its share of the tail's list
     if ((prefix + G - 1) / G + (F - prefix + G - 1) / G > kMaxShare) return false;
     if (G > kMaxG || r > kMaxRank || (r + G - 1) / G > kMaxP1R) return false;
-    if ((d / 4 + G - 1) / G > kNCT) return false;  // y initialisation: one float4 per consumer thread
+    if ((d / 4 + G - 1) / G > kNCW8 * 32) return false;  // y initialisation: one float4 per consumer thread
     if (!((wtype == 1 && ptype == 1) || (wtype == 2 && ptype == 1) || (wtype == 0 && ptype == 0))) return false;
     if ((F + G - 1) / G > kMaxRange) return false;
-    return chunks_per_thread(wtype, d) <= (wtype == 2 ? 2 : 8);
+    return chunks_per_thread(wtype, d, kNCW8) <= (wtype == 2 ? 2 : 8);
 }
 
 cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
@@ -1013,19 +1033,19 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     const uint32_t R = row_slot_bytes(a.wtype, a.d);
     uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
     sb = (sb + 127u) & ~127u;
-    const int need = chunks_per_thread(a.wtype, a.d);
+    const int need = chunks_per_thread(a.wtype, a.d, kNCW8);
     const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
     const size_t budget = (size_t)(colocate(epc, need) ? 110 : 226) * 1024;
     int ns = (int)((budget - kHdr) / sb);
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
     switch (a.wtype * 2 + (a.gated ? 1 : 0)) {
-    case 0: return launch_ch<0, float, false>(p, need, G, ns, sb, s);
-    case 1: return launch_ch<0, float, true>(p, need, G, ns, sb, s);
-    case 2: return launch_ch<1, __half, false>(p, need, G, ns, sb, s);
-    case 3: return launch_ch<1, __half, true>(p, need, G, ns, sb, s);
-    case 4: return launch_ch<2, __half, false>(p, need, G, ns, sb, s);
-    case 5: return launch_ch<2, __half, true>(p, need, G, ns, sb, s);
+    case 0: return launch_ch<0, float, false>(p, a.d, G, ns, sb, s);
+    case 1: return launch_ch<0, float, true>(p, a.d, G, ns, sb, s);
+    case 2: return launch_ch<1, __half, false>(p, a.d, G, ns, sb, s);
+    case 3: return launch_ch<1, __half, true>(p, a.d, G, ns, sb, s);
+    case 4: return launch_ch<2, __half, false>(p, a.d, G, ns, sb, s);
+    case 5: return launch_ch<2, __half, true>(p, a.d, G, ns, sb, s);
     default: return cudaErrorInvalidValue;
     }
 }
