@@ -84,18 +84,20 @@ __device__ __forceinline__ float2 h2f(unsigned u)
     return __half22float2(h);
 }
 
+// Two accumulator chains of four: a consumer warp has few neighbours on its
+// SM sub-partition to hide FMA latency behind, so a chain of 8 dependent FMAs
+// per chunk left it waiting.
 __device__ __forceinline__ float dot8_f16(uint4 w, const float *x)
 {
     float2 a = h2f(w.x), b = h2f(w.y), c = h2f(w.z), d = h2f(w.w);
-    float s = a.x * x[0];
-    s = fmaf(a.y, x[1], s);
-    s = fmaf(b.x, x[2], s);
-    s = fmaf(b.y, x[3], s);
-    s = fmaf(c.x, x[4], s);
-    s = fmaf(c.y, x[5], s);
-    s = fmaf(d.x, x[6], s);
-    s = fmaf(d.y, x[7], s);
-    return s;
+    float s0 = a.x * x[0], s1 = a.y * x[1];
+    s0 = fmaf(b.x, x[2], s0);
+    s1 = fmaf(b.y, x[3], s1);
+    s0 = fmaf(c.x, x[4], s0);
+    s1 = fmaf(c.y, x[5], s1);
+    s0 = fmaf(d.x, x[6], s0);
+    s1 = fmaf(d.y, x[7], s1);
+    return s0 + s1;
 }
 
 __device__ __forceinline__ float dot4_f32(uint4 w, const float *x)
