@@ -924,15 +924,25 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
         ++q;
     }
     if (!any) return;
-#pragma unroll
-    for (int u = 0; u < CH; ++u) {
+    // every CTA adds into all of y: odd CTAs go through their chunks in the
+    // opposite order, so that CTAs finishing together queue on fewer of the
+    // same lines of y
+    auto add = [&](int u, int e) {
         const int cc = t + kNCT * u;
-        if (cc < nch) {
+        if (cc < nch)
+            atomicAdd(reinterpret_cast<float4 *>(p.y + (size_t)cc * EPC + e),
+                      make_float4(acc[u][e], acc[u][e + 1], acc[u][e + 2], acc[u][e + 3]));
+    };
+    if ((c & 1) == 0) {
 #pragma unroll
-            for (int e = 0; e < EPC; e += 4)
-                atomicAdd(reinterpret_cast<float4 *>(p.y + (size_t)cc * EPC + e),
-                          make_float4(acc[u][e], acc[u][e + 1], acc[u][e + 2], acc[u][e + 3]));
-        }
+        for (int u = 0; u < CH; ++u)
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4) add(u, e);
+    } else {
+#pragma unroll
+        for (int u = CH - 1; u >= 0; --u)
+#pragma unroll
+            for (int e = EPC - 4; e >= 0; e -= 4) add(u, e);
     }
 }
 
