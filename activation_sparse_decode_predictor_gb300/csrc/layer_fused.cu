@@ -77,7 +77,7 @@ constexpr int kMaxShare = 512;     // FFN rows per CTA (share of the active list
 constexpr int kMaxRange = 512;     // neurons per CTA range (P2 rows)
 constexpr int kMaxG = 1024;
 constexpr int kMaxRank = 2048;
-constexpr int kGroup = 8;          // P2 rows per job
+constexpr int kGroup = 8;          // P2 rows per job (12 in the 12-warp variant when a stage holds them)
 constexpr int kMaxP1 = 8;          // P1 rows per job
 constexpr int kMaxP1R = 16;        // P1 rows per CTA (rank / #SMs)
 constexpr int kUpRing = 32;        // FFN up rows in flight (> ring stages)
@@ -217,11 +217,12 @@ __host__ __device__ constexpr bool colocate(int epc, int ch) { return PI_FUSED_C
 // it.  8 consumer warps + the producer put 3 warps on one sub-partition (at
 // most 170 registers a thread); 12 + 1 put 4 there, so that variant declares a
 // 512-thread bound, which caps it at 128 registers (it launches 416 threads).
-template <int WT, typename PT, bool GATED, int CH, int NCW>
+template <int WT, typename PT, bool GATED, int CH, int NCW, int KG>
 __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate(Fmt<WT>::EPC, CH) ? 2 : 1)
     k_layer_b1(FusedParams p, int nstages, uint32_t stage_bytes)
 {
     static_assert(NCW == kNCW8 || NCW == kMaxNCW, "8 or 12 consumer warps");
+    static_assert(KG == kGroup || (KG == 12 && NCW == kMaxNCW), "P2 jobs of 8 rows, or 12 with 12 warps");
     constexpr int kNCW = NCW;
     constexpr int kNCT = kNCW * 32;
     constexpr int kThreads = kNCT + 32;
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
     const uint32_t p1row = (uint32_t)d * sizeof(PT), p2row = (uint32_t)r * sizeof(PT);
     const int rp1 = max(1, min(kMaxP1, (int)(stage_bytes / p1row)));  // P1 rows per job
     const int nP1 = (nP1r + rp1 - 1) / rp1;
-    const int nP2 = (nR + kGroup - 1) / kGroup;
+    const int nP2 = (nR + KG - 1) / KG;
     // No ordered active list requested: the FFN rows come from a shared work
     // queue that every CTA feeds with its range's active neurons, so there is
     // no second grid barrier, no prefix scan and no share lookup, and idle CTAs
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
                     // the ring is full: ask L2 for the P2 rows still to come, so
                     // later refills do not wait for HBM (issued after the ring's
                     // own copies so those are served first)
-                    const int gnext = j0 + max(0, i - nP1) * kGroup;
+                    const int gnext = j0 + max(0, i - nP1) * KG;
                     (void)gnext;
                 }
                 if (!acquire(q)) {
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
                     mbar_arrive_expect_tx(&T.full[s], bytes);
                     bulk_g2s_once(st, p.p1 + (size_t)k0 * p1row, bytes, &T.full[s], pol);
                 } else {
-                    const int g0 = j0 + (i - nP1) * kGroup, g1 = min(g0 + kGroup, j1);
+                    const int g0 = j0 + (i - nP1) * KG, g1 = min(g0 + KG, j1);
                     const uint32_t bytes = (uint32_t)(g1 - g0) * p2row;
                     T.job[s] = make_int4(kJobP2, g0, g1, 0);
                     mbar_arrive_expect_tx(&T.full[s], bytes);
@@ -650,7 +651,7 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
     //         (up to 8 rows) round-robin, keeps all rows in flight, and reduces
     //         the rows together with one transposed butterfly (9 shuffles) ----
     {
-        static_assert(kGroup == 8, "butterfly below reduces 8 rows");
+        static_assert(kGroup == 8, "butterfly below reduces 8 rows (and a second one 4 more)");
         // Rounds of m <= #stages jobs, one per warp, with a consumer barrier
         // between rounds: a stage's previous job is then always released
         // before anyone waits on its next one, so a parity wait never looks
@@ -671,17 +672,18 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
             const uint8_t *st = stages + (size_t)s * stage_bytes;
             const int4 job = T.job[s];
             const int nrow = job.z - job.y;
-            // All 8 rows, branch-free, so their loads and FMA chains
+            // All KG rows, branch-free, so their loads and FMA chains
             // interleave: rows past nrow read stage bytes that are in bounds
-            // and are discarded; chunks past the row end load zeros.
-            float v[kGroup];
+            // (a stage holds KG rows) and are discarded; chunks past the row
+            // end load zeros.
+            float v[KG];
 #pragma unroll
-            for (int rr = 0; rr < kGroup; ++rr) v[rr] = 0.f;
+            for (int rr = 0; rr < KG; ++rr) v[rr] = 0.f;
 #pragma unroll
             for (int u = 0; u < kHreg; ++u) {
                 const bool in = lane + 32 * u < nc2;
 #pragma unroll
-                for (int rr = 0; rr < kGroup; ++rr) {
+                for (int rr = 0; rr < KG; ++rr) {
                     uint4 w = make_uint4(0u, 0u, 0u, 0u);
                     if (in) w = *reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)(lane + 32 * u) * 16);
                     v[rr] += dot16<PT>(w, hreg[u]);
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
             }
             for (int cc = lane + 32 * kHreg; cc < nc2; cc += 32) {  // ranks above 32*kHreg*PEPC
 #pragma unroll
-                for (int rr = 0; rr < kGroup; ++rr)
+                for (int rr = 0; rr < KG; ++rr)
                     v[rr] += dot16<PT>(*reinterpret_cast<const uint4 *>(st + (size_t)rr * p2row + (size_t)cc * 16),
                                        &T.hs[cc * PEPC]);
             }
@@ -710,6 +712,25 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
             const int rr = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
             if ((lane & 3) == 0 && rr < nrow) T.lg[job.y + rr - j0] = v[0] + T.pb[job.y + rr - j0];
+            if constexpr (KG == 12) {
+                // rows 8..11: the same exchange over bits 4 and 3 (lane l then
+                // holds row 8 + 2*b4 + b3), then three steps finish the sum
+#pragma unroll
+                for (int m = 16, n = 2; m >= 8; m >>= 1, n >>= 1) {
+                    const bool upper = (lane & m) != 0;
+#pragma unroll
+                    for (int k = 0; k < n; ++k) {
+                        const float send = upper ? v[8 + k] : v[8 + k + n];
+                        const float keep = upper ? v[8 + k + n] : v[8 + k];
+                        v[8 + k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    }
+                }
+                v[8] += __shfl_xor_sync(0xffffffffu, v[8], 4);
+                v[8] += __shfl_xor_sync(0xffffffffu, v[8], 2);
+                v[8] += __shfl_xor_sync(0xffffffffu, v[8], 1);
+                const int r4 = 8 + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+                if ((lane & 7) == 0 && r4 < nrow) T.lg[job.y + r4 - j0] = v[8] + T.pb[job.y + r4 - j0];
+            }
             // the stage's empty barrier counts one arrival per consumer warp:
             // this warp consumed it alone, so it arrives for all of them
             __syncwarp();
@@ -946,10 +967,10 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
     }
 }
 
-template <int WT, typename PT, bool GATED, int CH, int NCW>
+template <int WT, typename PT, bool GATED, int CH, int NCW, int KG = kGroup>
 cudaError_t launch_t(const FusedParams &p, int G, int ns, uint32_t stage_bytes, cudaStream_t s)
 {
-    auto k = k_layer_b1<WT, PT, GATED, CH, NCW>;
+    auto k = k_layer_b1<WT, PT, GATED, CH, NCW, KG>;
     const size_t smem = kHdr + (size_t)ns * stage_bytes;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -966,15 +987,22 @@ int chunks_per_thread(int wtype, int d, int ncw)
     return (d / epc + ncw * 32 - 1) / (ncw * 32);
 }
 
+// kg12: a stage holds 12 P2 rows (then the 12-warp variant takes P2 jobs of
+// 12 rows: half as many bytes again in flight in the logits phase, with 12
+// warps to take them)
 template <int WT, typename PT, bool GATED>
-cudaError_t launch_ch(const FusedParams &p, int d, int G, int ns, uint32_t sb, cudaStream_t s)
+cudaError_t launch_ch(const FusedParams &p, int d, bool kg12, int G, int ns, uint32_t sb, cudaStream_t s)
 {
     const int need = chunks_per_thread(WT, d, kNCW8);
     if constexpr (WT != 2) {
         if (need >= 6) {  // the widest rows: 12 consumer warps, 4-6 chunks a thread
             const int need12 = chunks_per_thread(WT, d, kMaxNCW);
-            if (need12 <= 4) return launch_t<WT, PT, GATED, 4, kMaxNCW>(p, G, ns, sb, s);
-            if (need12 <= 6) return launch_t<WT, PT, GATED, 6, kMaxNCW>(p, G, ns, sb, s);
+            if (need12 <= 4)
+                return kg12 ? launch_t<WT, PT, GATED, 4, kMaxNCW, 12>(p, G, ns, sb, s)
+                            : launch_t<WT, PT, GATED, 4, kMaxNCW>(p, G, ns, sb, s);
+            if (need12 <= 6)
+                return kg12 ? launch_t<WT, PT, GATED, 6, kMaxNCW, 12>(p, G, ns, sb, s)
+                            : launch_t<WT, PT, GATED, 6, kMaxNCW>(p, G, ns, sb, s);
         }
     }
     if (need <= 1) return launch_t<WT, PT, GATED, 1, kNCW8>(p, G, ns, sb, s);
@@ -1042,6 +1070,7 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     const int esz = a.ptype == 1 ? 2 : 4;
     const uint32_t R = row_slot_bytes(a.wtype, a.d);
     uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});
+    const bool kg12 = 12u * (uint32_t)a.r * esz <= std::max<uint32_t>((uint32_t)a.d * esz, (a.gated ? 2u : 1u) * R);
     sb = (sb + 127u) & ~127u;
     const int need = chunks_per_thread(a.wtype, a.d, kNCW8);
     const int epc = a.wtype == 0 ? 4 : (a.wtype == 1 ? 8 : 32);
@@ -1050,12 +1079,12 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     ns = std::max(2, std::min(ns, kMaxStages));
     if (kHdr + (size_t)ns * sb > 227 * 1024) return cudaErrorNotSupported;
     switch (a.wtype * 2 + (a.gated ? 1 : 0)) {
-    case 0: return launch_ch<0, float, false>(p, a.d, G, ns, sb, s);
-    case 1: return launch_ch<0, float, true>(p, a.d, G, ns, sb, s);
-    case 2: return launch_ch<1, __half, false>(p, a.d, G, ns, sb, s);
-    case 3: return launch_ch<1, __half, true>(p, a.d, G, ns, sb, s);
-    case 4: return launch_ch<2, __half, false>(p, a.d, G, ns, sb, s);
-    case 5: return launch_ch<2, __half, true>(p, a.d, G, ns, sb, s);
+    case 0: return launch_ch<0, float, false>(p, a.d, kg12, G, ns, sb, s);
+    case 1: return launch_ch<0, float, true>(p, a.d, kg12, G, ns, sb, s);
+    case 2: return launch_ch<1, __half, false>(p, a.d, kg12, G, ns, sb, s);
+    case 3: return launch_ch<1, __half, true>(p, a.d, kg12, G, ns, sb, s);
+    case 4: return launch_ch<2, __half, false>(p, a.d, kg12, G, ns, sb, s);
+    case 5: return launch_ch<2, __half, true>(p, a.d, kg12, G, ns, sb, s);
     default: return cudaErrorInvalidValue;
     }
 }
