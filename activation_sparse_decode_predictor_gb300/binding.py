@@ -156,8 +156,8 @@ class Layer:
                             _p(p2), _p(p_bias), None, int(dense_prefix))
 
     def set_next(self, other: "Layer | None"):
-        """Name the layer run next on the same stream (its predictor weights are
-        asked into L2 during this layer's FFN phase), or None."""
+        """Name the layer run next on the same stream (a scheduling hint the
+        current kernels do not use), or None."""
         self._next = other
         self.desc.next = ctypes.addressof(other.desc) if other is not None else None
 

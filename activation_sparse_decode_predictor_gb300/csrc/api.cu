@@ -393,17 +393,6 @@ pi_status ffn_layer(const pi_ffn_desc *desc, const float *x, const float *x_prev
         a.d = desc->d_model;
         a.F = desc->d_ff;
         a.prefix = desc->dense_prefix;
-        if (const pi_ffn_desc *nx = desc->next) {
-            // the next layer's P1 (its first phase waits on it); its P2 is pulled
-            // into L2 by that layer's own kernel early enough.  A bulk prefetch
-            // wants a 16-byte aligned start: a misaligned P1 is not prefetched.
-            const size_t pe = nx->ptype == PI_F16 ? 2 : 4;
-            if (nx->p1 && al(nx->p1, 16) && nx->rank > 0 && nx->rank % 8 == 0 && nx->d_model > 0 &&
-                nx->d_model % 8 == 0) {
-                a.pf[0] = nx->p1;
-                a.pf_bytes[0] = (size_t)nx->rank * nx->d_model * pe;
-            }
-        }
         return cuda_status(launch_layer_b1(a, s));
     }
     if (chained && launch_rms_residual(x_prev, y_prev, batch, desc->d_model, const_cast<float *>(x), s) != cudaSuccess)

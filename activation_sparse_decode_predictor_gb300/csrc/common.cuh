@@ -240,8 +240,8 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, unsigned parity, u
 }
 
 // L2 evict-first policy for weights that one decode step reads once, so their
-// lines leave L2 before data that is read again (the next layer's predictor
-// rows asked into L2 ahead of time, activations, the control block).  Made
+// lines leave L2 before data that is read again (activations, the work queue,
+// the control block).  Made
 // once per issuing thread: createpolicy is an instruction of its own, and a
 // producer that made it before every copy paid for it on each one.
 __device__ __forceinline__ unsigned long long evict_first_policy()

@@ -154,8 +154,6 @@ struct LayerB1Args {
     WsCtrl *ctrl;
     int d, F;
     int prefix;             // neurons [0, prefix) always active (no predictor rows read for them)
-    const void *pf[2];      // regions asked into L2 during the FFN phase (the next layer's P1), or null
-    size_t pf_bytes[2];
 };
 bool fused_layer_supported(int wtype, int ptype, int d, int F, int r, int prefix);
 cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s);

@@ -12,7 +12,7 @@
 // is read.
 //
 // GB300 design.  One CTA per SM (all CTAs resident together), 1 producer warp
-// + 8 consumer warps.  The producer thread streams every byte the CTA needs
+// + 8 (or 12) consumer warps.  The producer thread streams every byte the CTA needs
 // through one ring of shared-memory stages with 1-D bulk copies completing on
 // mbarriers, in job order:
 //   P1 jobs      consecutive rows of this CTA's share of the predictor's P1,
@@ -20,8 +20,8 @@
 //   FFN jobs     up/gate rows of this CTA's share of the active neurons, and
 //                the down row of each neuron whose activation is non-zero.
 // Every weight copy carries an L2 evict-first policy: a decode step reads each
-// weight byte once, and those lines must not push out what is read again (the
-// next layer's P1, asked into L2 during this layer's FFN phase).  On entry,
+// weight byte once, and those lines must not push out what is read again
+// (activations, the queue, the control block).  On entry,
 // before the programmatic-dependent-launch wait, the producer fills the ring
 // with P1 and P2 rows (they do not depend on the previous kernel).  The
 // consumers:
@@ -199,8 +199,6 @@ struct FusedParams {
     int queue;
     int prefix;          // neurons [0, prefix) always active; the predictor covers [prefix, F)
     float tau;
-    const uint8_t *pf[2];  // the next layer's predictor weights (or null), asked into L2
-    size_t pf_bytes[2];
 };
 
 // Default: one CTA per SM with a deep ring.  With PI_FUSED_COLOCATE, narrow
@@ -341,7 +339,6 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
             }
             volatile int *state = T.state;
             int up = 0, ds = 0;
-            bool pf_done = false;
             bool exhausted = !qmode;  // queue mode: more rows may still be published
             int pend = -1, pk = 0;    // queue batch taken: slots [pend + pk, pend + kQTake) not read yet
             long long qspins = 0;
@@ -446,19 +443,6 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
                     mbar_arrive(&T.full[s]);
                 }
                 ++q;
-                if (!pf_done && exhausted && up >= sn) {
-                    // every up row of the share is requested: while the rest of the
-                    // FFN phase runs on them, ask L2 for this CTA's slice of the
-                    // next layer's P1 (the next kernel's first phase waits on it)
-                    pf_done = true;
-                    for (int k = 0; k < 2; ++k) {
-                        if (!p.pf[k] || p.pf_bytes[k] == 0) continue;
-                        const size_t per = ((p.pf_bytes[k] + G - 1) / G + 15) & ~(size_t)15;
-                        const size_t off = (size_t)c * per;
-                        if (off < p.pf_bytes[k])
-                            prefetch_l2(p.pf[k] + off, (uint32_t)min(per, p.pf_bytes[k] - off));
-                    }
-                }
                 if (kind == kJobEnd) break;
             }
             if (failed) {  // never leave bulk copies in flight into this CTA's shared memory
@@ -1063,10 +1047,6 @@ cudaError_t launch_layer_b1(const LayerB1Args &a, cudaStream_t s)
     p.tau = a.tau;
     p.queue = (!a.idx_out && !a.n_active && (long long)a.F <= (long long)(kMaxShare - kQTake + 1) * G) ? 1 : 0;
     p.prefix = a.prefix;
-    for (int k = 0; k < 2; ++k) {
-        p.pf[k] = static_cast<const uint8_t *>(a.pf[k]);
-        p.pf_bytes[k] = a.pf[k] ? a.pf_bytes[k] : 0;
-    }
     const int esz = a.ptype == 1 ? 2 : 4;
     const uint32_t R = row_slot_bytes(a.wtype, a.d);
     uint32_t sb = std::max<uint32_t>({(uint32_t)a.d * esz, (uint32_t)kGroup * a.r * esz, (a.gated ? 2u : 1u) * R});

@@ -260,8 +260,7 @@ def setup_ours(w, replicas, dev, prefix="0"):
         Lk = {key: (v.clone() if isinstance(v, torch.Tensor) else v) for key, v in L0.items()}
         reps.append((Lk, B.Layer.from_dict(Lk)))
     # consecutive calls run consecutive copies, as a decode step runs consecutive
-    # layers: each copy names the one after it (its predictor P1 is asked into L2
-    # during this copy's FFN phase)
+    # layers: each copy names the one after it (a scheduling hint)
     for k in range(replicas):
         reps[k][1].set_next(reps[(k + 1) % replicas][1])
     X = synth.workload_tokens(w, device=f"cuda:{dev}")

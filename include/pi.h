@@ -122,11 +122,11 @@ typedef struct pi_ffn_desc_s {
     const void *p2;
     const float *p_bias;
     /* Optional (NULL: none): the layer the caller runs next on the same stream.
-     * pi_ffn_layer at batch 1 asks L2 for that layer's predictor P1 while its
-     * own sparse FFN phase runs, so the next call's first phase finds it on
-     * chip; only the host reads *next (pointers and shape; a P1 not 16-byte
-     * aligned is skipped).  Layer-by-layer decode knows its next layer; the
-     * weights are still read from HBM once. */
+     * A scheduling hint that the current kernels do not use: asking L2 for
+     * that layer's predictor P1 during this layer's sparse FFN phase was
+     * measured slower on GB300 (the rows did not reach the next layer's SMs
+     * faster, and the request took HBM time from this layer's tail).  The
+     * library never reads *next. */
     const struct pi_ffn_desc_s *next;
     /* Always-on prefix: neurons [0, dense_prefix) of the storage order are
      * active at every step whatever the predictor says, and their rows of p2

@@ -339,10 +339,10 @@ def test_layer_and_predict_share_a_workspace():
         assert all(amb[j] for j in got ^ ref)
 
 
-def test_next_layer_prefetch_changes_nothing():
-    """Naming the next layer only asks L2 for its predictor weights: outputs and
-    active lists stay those of the oracle, including with a misaligned (so not
-    prefetched) or self-referencing next layer."""
+def test_next_layer_hint_changes_nothing():
+    """Naming the next layer is a scheduling hint the kernels do not use:
+    outputs and active lists stay those of the oracle with another, a
+    self-referencing or no next layer."""
     d, F, r = 512, 3000, 64
     lay, olay, H = _layer(d, F, r, True, "f16", seed=97)
     lay2, _, _ = _layer(d, F, r, False, "f16", seed=98)
