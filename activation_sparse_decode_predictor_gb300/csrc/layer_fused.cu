@@ -12,11 +12,12 @@
 // is read.
 //
 // GB300 design.  One CTA per SM (all CTAs resident together), 1 producer warp
-// + 8 (or 12) consumer warps.  The producer thread streams every byte the CTA needs
-// through one ring of shared-memory stages with 1-D bulk copies completing on
-// mbarriers, in job order:
+// + 8 consumer warps (12 for rows of 12 Ki fp16 columns or more).  The producer
+// thread streams every byte the CTA needs through one ring of shared-memory
+// stages with 1-D bulk copies completing on mbarriers, in job order:
 //   P1 jobs      consecutive rows of this CTA's share of the predictor's P1,
-//   P2 jobs      8 rows of P2 each, for this CTA's contiguous neuron range,
+//   P2 jobs      8 rows of P2 each (12 in the 12-warp variant when a stage
+//                holds them), for this CTA's contiguous neuron range,
 //   FFN jobs     up/gate rows of this CTA's share of the active neurons, and
 //                the down row of each neuron whose activation is non-zero.
 // Every weight copy carries an L2 evict-first policy: a decode step reads each
