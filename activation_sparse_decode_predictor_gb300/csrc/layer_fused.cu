@@ -868,27 +868,54 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
             break;
         }
         const uint8_t *st = stages + (size_t)s * stage_bytes;
+        bool two = false;  // this pass also took the next job (an up row that has landed)
+        int s2 = 0;
         if (job.x == kJobUp) {
+            // 12-warp variant: the next job too, when it is an up row whose
+            // data has already landed; both rows go through one dot pass and
+            // one round of reductions, which halves the fixed cost per row.
+            // (The test looks one use ahead on that stage, as the next wait
+            // would.  Measured: faster with 12 warps, slower with 8.)
+            int4 job2 = make_int4(0, 0, 0, 0);
+            if constexpr (kNCW == kMaxNCW) {
+                const int q2 = q + 1;
+                s2 = q2 % nstages;
+                if (__all_sync(0xffffffffu, mbar_test_wait(&T.full[s2], (unsigned)(q2 / nstages) & 1u)))
+                    job2 = T.job[s2];
+            }
+            two = job2.x == kJobUp;
+            const uint8_t *st2 = stages + (size_t)s2 * stage_bytes;
             // the row's bias: from the share table, or (queue mode) from b_act,
             // loaded now and used by the warp that finishes the row
-            float bj = 0.f;
-            if (lane == 0) bj = qmode ? (p.b_act ? __ldg(p.b_act + job.z) : 0.f) : T.bias[job.y];
-            float pa = 0.f, pu = 0.f;
+            float bj = 0.f, bj2 = 0.f;
+            if (lane == 0) {
+                bj = qmode ? (p.b_act ? __ldg(p.b_act + job.z) : 0.f) : T.bias[job.y];
+                if (two) bj2 = qmode ? (p.b_act ? __ldg(p.b_act + job2.z) : 0.f) : T.bias[job2.y];
+            }
+            float pa = 0.f, pu = 0.f, pa2 = 0.f, pu2 = 0.f;
 #pragma unroll
             for (int u = 0; u < CH; ++u) {
                 const int cc = t + kNCT * u;
                 if (cc < nch) {
                     pa += chunk_dot<WT>(st, cc, d, xr[u]);
                     if constexpr (GATED) pu += chunk_dot<WT>(st + R, cc, d, xr[u]);
+                    if (two) {
+                        pa2 += chunk_dot<WT>(st2, cc, d, xr[u]);
+                        if constexpr (GATED) pu2 += chunk_dot<WT>(st2 + R, cc, d, xr[u]);
+                    }
                 }
             }
             pa = warp_sum(pa);
             if constexpr (GATED) pu = warp_sum(pu);
-            if (lane == 0) {
-                // the last warp to contribute finishes the row: no CTA barrier
-                const int e = job.y & (kUpRing - 1);
-                T.redu[e][warp][0] = pa;
-                T.redu[e][warp][1] = pu;
+            if (two) {
+                pa2 = warp_sum(pa2);
+                if constexpr (GATED) pu2 = warp_sum(pu2);
+            }
+            // the last warp to contribute to a row finishes it: no CTA barrier
+            auto finish = [&](const int4 &jb, float va, float vu, float b) {
+                const int e = jb.y & (kUpRing - 1);
+                T.redu[e][warp][0] = va;
+                T.redu[e][warp][1] = vu;
                 __threadfence_block();
                 if (atomicAdd(&T.upcnt[e], 1) == kNCW - 1) {
                     __threadfence_block();
@@ -899,12 +926,16 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
                         uu += T.redu[e][w][1];
                     }
                     T.upcnt[e] = 0;
-                    float a = activate(p.act, z + bj);
+                    float a = activate(p.act, z + b);
                     if constexpr (GATED) a *= uu;
-                    T.a[job.y] = a;
+                    T.a[jb.y] = a;
                     __threadfence_block();
-                    *reinterpret_cast<volatile int *>(&T.state[job.y]) = (a != 0.f) ? 2 : 1;
+                    *reinterpret_cast<volatile int *>(&T.state[jb.y]) = (a != 0.f) ? 2 : 1;
                 }
+            };
+            if (lane == 0) {
+                finish(job, pa, pu, bj);
+                if (two) finish(job2, pa2, pu2, bj2);
             }
         } else {
             const float a = T.a[job.y];
@@ -917,6 +948,10 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
         }
         release(s);
         ++q;
+        if (two) {
+            release(s2);
+            ++q;
+        }
     }
     if (!any) return;
     // every CTA adds into all of y: odd CTAs go through their chunks in the
