@@ -89,3 +89,26 @@ def test_measured_peaks_file(tmp_path, monkeypatch, content, want):
         assert (peak, src) == (bench.FALLBACK_HBM_GBS, "fallback")
     else:
         assert (peak, src) == (want, "measured")
+
+
+def test_committed_traffic_only_for_the_current_kernel_source(tmp_path, monkeypatch):
+    """A profile summary's DRAM traffic is used only while its recorded source
+    hash matches the kernel sources as they are now; a stale or missing hash,
+    or no summary, gives None (the bench line then reports traffic null)."""
+    csrc = tmp_path / "activation_sparse_decode_predictor_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES["k_layer_b1"]:
+        (csrc / f).write_text(f"// {f}\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash("k_layer_b1")
+    assert len(h) == 16
+    prof = tmp_path / "profiles" / "k_layer_b1_wl.md"
+    assert bench.committed_traffic("k_layer_b1", "wl") is None
+    prof.write_text(f"text\ntraffic_bytes_per_launch: 213.1e6\nkernel_source_sha: {h}\n")
+    assert bench.committed_traffic("k_layer_b1", "wl") == 213.1e6
+    prof.write_text("traffic_bytes_per_launch: 213.1e6\nkernel_source_sha: 0123456789abcdef\n")
+    assert bench.committed_traffic("k_layer_b1", "wl") is None
+    prof.write_text(f"traffic_bytes_per_launch: 213.1e6\nkernel_source_sha: {h}\n")
+    (csrc / "layer_fused.cu").write_text("// changed\n")  # the kernel changed after the capture
+    assert bench.committed_traffic("k_layer_b1", "wl") is None
