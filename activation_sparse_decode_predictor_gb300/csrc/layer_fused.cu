@@ -622,8 +622,9 @@ __global__ void __launch_bounds__(NCW == kNCW8 ? kNCW8 * 32 + 32 : 512, colocate
         for (int e = 0; e < PEPC; ++e) hreg[u][e] = (lane + 32 * u < nc2) ? T.hs[(lane + 32 * u) * PEPC + e] : 0.f;
 
     // ---- 2. logits of this CTA's neuron range: each warp takes whole P2 jobs
-    //         (up to 8 rows) round-robin, keeps all rows in flight, and reduces
-    //         the rows together with one transposed butterfly (9 shuffles) ----
+    //         (up to KG rows) round-robin, keeps all rows in flight, and reduces
+    //         them with one transposed butterfly (9 shuffles for 8 rows; 6 more
+    //         for rows 8-11 of a 12-row job) ----
     {
         static_assert(kGroup == 8, "butterfly below reduces 8 rows (and a second one 4 more)");
         // Rounds of m <= #stages jobs, one per warp, with a consumer barrier
